@@ -1,0 +1,249 @@
+"""Thin Python binding of libattn.so (the C ABI in include/attn.h).
+
+Argument marshalling only: every step of the attention path runs in the
+library's CUDA kernels.  Tensors are torch CUDA tensors (device memory and
+streams are PyTorch's); the functions check dtypes, shapes, devices and
+contiguity, build the ``attn_shape`` struct and call the entry point of the
+same name on the current stream (or the one given).  There is no fallback:
+if the library is missing or a call fails, an exception is raised.
+"""
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_LIB_PATH = _build.LIB
+
+ATTN_OK = 0
+ATTN_ERR_SHAPE = -1
+ATTN_ERR_NULL = -2
+ATTN_ERR_ALIGN = -3
+ATTN_ERR_WORKSPACE = -4
+ATTN_ERR_CUDA = -5
+ATTN_ERR_DEVICE_TIMEOUT = -6
+ATTN_ERR_DEVICE = -7
+
+HEAD_DIM = 64
+
+
+class AttnShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("seq", ctypes.c_int32),
+                ("heads", ctypes.c_int32), ("kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("causal", ctypes.c_int32),
+                ("seq_lens", ctypes.c_void_p), ("scale", ctypes.c_float),
+                ("head_begin", ctypes.c_int32), ("head_count", ctypes.c_int32)]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (fn, error_string(code), code))
+
+
+_lib = None
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libattn.so (built in-tree by ``build.py``); raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError("libattn.so not found at %s: build it with "
+                          "causal_streaming_softmax_gb300.build.build()" % p)
+    lib = ctypes.CDLL(p)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    sp = ctypes.POINTER(AttnShape)
+    lib.attn_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp]
+    lib.attn_row_terms.argtypes = [sp, vp, vp, vp, vp]
+    lib.attn_bwd_workspace_bytes.argtypes = [sp]
+    lib.attn_bwd_workspace_bytes.restype = sz
+    lib.attn_bwd_keys.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+    lib.attn_bwd_queries.argtypes = [sp, vp, vp, sz, vp, vp]
+    lib.attn_error_string.argtypes = [ctypes.c_int]
+    lib.attn_error_string.restype = ctypes.c_char_p
+    lib.attn_last_device_error.argtypes = [vp]
+    lib.attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.attn_set_wait_limit_ns.restype = None
+    lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    lib.attn_version.restype = ctypes.c_int
+    for name in ("attn_fwd", "attn_row_terms", "attn_bwd_keys", "attn_bwd_queries",
+                 "attn_last_device_error", "attn_selftest_wait_timeout"):
+        getattr(lib, name).restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def error_string(code: int) -> str:
+    return load_library().attn_error_string(int(code)).decode()
+
+
+def _check(fn, rc):
+    if rc != ATTN_OK:
+        raise AttnError(fn, rc)
+
+
+@dataclass
+class Shape:
+    """Problem shape; ``seq_lens`` is an int32 CUDA tensor [batch] or None."""
+    batch: int
+    seq: int
+    heads: int
+    kv_heads: int
+    causal: bool = True
+    scale: float = 0.125
+    seq_lens: Optional[torch.Tensor] = None
+    head_begin: int = 0
+    head_count: int = 0
+
+    def c_struct(self) -> AttnShape:
+        lens = 0
+        if self.seq_lens is not None:
+            t = self.seq_lens
+            if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous() \
+                    or t.numel() != self.batch:
+                raise ValueError("seq_lens must be a contiguous int32 CUDA tensor [batch]")
+            lens = t.data_ptr()
+        return AttnShape(self.batch, self.seq, self.heads, self.kv_heads, HEAD_DIM,
+                         1 if self.causal else 0, lens, float(self.scale),
+                         self.head_begin, self.head_count)
+
+    def chunk(self, head_begin: int, head_count: int) -> "Shape":
+        return Shape(self.batch, self.seq, self.heads, self.kv_heads, self.causal, self.scale,
+                     self.seq_lens, head_begin, head_count)
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _want(t: torch.Tensor, name: str, dtype, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def attn_fwd(s: Shape, q, k, vt, o, lse, stream=None) -> None:
+    B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
+    args = (_want(q, "q", torch.float16, (B, H, T, 64)),
+            _want(k, "k", torch.float16, (B, Hkv, T, 64)),
+            _want(vt, "vt", torch.float16, (B, Hkv, 64, T)),
+            _want(o, "o", torch.float16, (B, T, H * 64)),
+            _want(lse, "lse", torch.float32, (B, H, T)))
+    shape = s.c_struct()
+    _check("attn_fwd", load_library().attn_fwd(ctypes.byref(shape), *args, _stream_ptr(stream)))
+
+
+def attn_row_terms(s: Shape, o, dout, delta, stream=None) -> None:
+    B, T, H = s.batch, s.seq, s.heads
+    args = (_want(o, "o", torch.float16, (B, T, H * 64)),
+            _want(dout, "dout", torch.float16, (B, H, T, 64)),
+            _want(delta, "delta", torch.float32, (B, H, T)))
+    shape = s.c_struct()
+    _check("attn_row_terms",
+           load_library().attn_row_terms(ctypes.byref(shape), *args, _stream_ptr(stream)))
+
+
+def workspace_bytes(s: Shape) -> int:
+    shape = s.c_struct()
+    n = load_library().attn_bwd_workspace_bytes(ctypes.byref(shape))
+    if n == 0:
+        raise AttnError("attn_bwd_workspace_bytes", ATTN_ERR_SHAPE)
+    return n
+
+
+def alloc_workspace(s: Shape, device=None) -> torch.Tensor:
+    """A uint8 CUDA tensor large enough for the dS workspace of ``s``."""
+    return torch.empty(workspace_bytes(s), dtype=torch.uint8,
+                       device=device or torch.device("cuda"))
+
+
+def _chunk_heads(s: Shape):
+    count = s.head_count or s.kv_heads
+    return s.head_begin, count
+
+
+def attn_bwd_keys(s: Shape, q, k, vt, dout, lse, delta, ws, dk, dvt, stream=None) -> None:
+    B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
+    if not (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.dtype == torch.uint8
+            and ws.is_contiguous()):
+        raise TypeError("ws must be a contiguous uint8 CUDA tensor")
+    args = (_want(q, "q", torch.float16, (B, H, T, 64)),
+            _want(k, "k", torch.float16, (B, Hkv, T, 64)),
+            _want(vt, "vt", torch.float16, (B, Hkv, 64, T)),
+            _want(dout, "dout", torch.float16, (B, H, T, 64)),
+            _want(lse, "lse", torch.float32, (B, H, T)),
+            _want(delta, "delta", torch.float32, (B, H, T)),
+            ws.data_ptr(), ws.numel(),
+            _want(dk, "dk", torch.float32, (B, Hkv, T, 64)),
+            _want(dvt, "dvt", torch.float32, (B, Hkv, 64, T)))
+    shape = s.c_struct()
+    _check("attn_bwd_keys",
+           load_library().attn_bwd_keys(ctypes.byref(shape), *args, _stream_ptr(stream)))
+
+
+def attn_bwd_queries(s: Shape, k, ws, dq, stream=None) -> None:
+    B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
+    if not (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.dtype == torch.uint8
+            and ws.is_contiguous()):
+        raise TypeError("ws must be a contiguous uint8 CUDA tensor")
+    args = (_want(k, "k", torch.float16, (B, Hkv, T, 64)), ws.data_ptr(), ws.numel(),
+            _want(dq, "dq", torch.float32, (B, H, T, 64)))
+    shape = s.c_struct()
+    _check("attn_bwd_queries",
+           load_library().attn_bwd_queries(ctypes.byref(shape), *args, _stream_ptr(stream)))
+
+
+def last_device_error(stream=None) -> int:
+    return load_library().attn_last_device_error(_stream_ptr(stream))
+
+
+def check_device_error(stream=None) -> None:
+    _check("device", last_device_error(stream))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    load_library().attn_set_wait_limit_ns(int(ns))
+
+
+def selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None) -> int:
+    return load_library().attn_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream))
+
+
+class Buffers:
+    """Device buffers of one forward + backward problem (boundary layouts)."""
+
+    def __init__(self, s: Shape, device=None):
+        dev = device or torch.device("cuda")
+        B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
+        self.o = torch.empty((B, T, H * 64), dtype=torch.float16, device=dev)
+        self.lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+        self.delta = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+        self.dq = torch.empty((B, H, T, 64), dtype=torch.float32, device=dev)
+        self.dk = torch.empty((B, Hkv, T, 64), dtype=torch.float32, device=dev)
+        self.dvt = torch.empty((B, Hkv, 64, T), dtype=torch.float32, device=dev)
+        self.ws = alloc_workspace(s, dev)
+
+
+def forward_backward(s: Shape, q, k, vt, dout, bufs: Buffers, stream=None) -> Buffers:
+    """One pass of the whole path: attn_fwd, attn_row_terms, attn_bwd_keys, attn_bwd_queries."""
+    attn_fwd(s, q, k, vt, bufs.o, bufs.lse, stream)
+    attn_row_terms(s, bufs.o, dout, bufs.delta, stream)
+    attn_bwd_keys(s, q, k, vt, dout, bufs.lse, bufs.delta, bufs.ws, bufs.dk, bufs.dvt, stream)
+    attn_bwd_queries(s, k, bufs.ws, bufs.dq, stream)
+    return bufs

@@ -1,0 +1,59 @@
+// attn_internal.h - what the host API hands the kernel launchers: the
+// validated shape with its derived sizes, and per-device context.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "attn.h"
+
+namespace css {
+
+// Tile edge shared by every kernel: 128 queries by 128 keys.  The dS
+// workspace is a sequence of such tiles (32 KiB of binary16 each).
+constexpr int kTile = 128;
+constexpr uint32_t kDsTileBytes = kTile * kTile * 2;
+
+struct Dims {
+  int B, T, H, Hkv, G;
+  int causal;
+  const int32_t* lens;  // device [B] or null
+  float scale;          // natural scale s
+  float c;              // fp32(s / ln 2)
+  int kv_begin;         // head chunk (backward calls)
+  int kv_count;
+  int nt;               // ceil(T / 128)
+  long long npairs;     // workspace tiles per query head
+  // workspace tile index of (query tile i, key tile j)
+  __host__ __device__ long long pair(int i, int j) const {
+    return causal ? (long long)i * (i + 1) / 2 + j : (long long)i * nt + j;
+  }
+};
+
+struct DevCtx {
+  uint32_t* err;     // device error word
+  uint64_t wait_ns;  // bounded-wait limit
+  int sm_count;
+};
+
+// Encodes a rank-3 binary16 tiled tensor map with the 128-byte swizzle.
+// dims/strides as cuTensorMapEncodeTiled takes them (strides in bytes of
+// dims 1 and 2), box = {box0, box1, 1}.
+bool encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                    uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1);
+
+int launch_fwd(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16_t* k,
+               const uint16_t* vt, uint16_t* o, float* lse, cudaStream_t stream);
+int launch_row_terms(const Dims& d, const DevCtx& ctx, const uint16_t* o, const uint16_t* dout,
+                     float* delta, cudaStream_t stream);
+int launch_bwd_keys(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16_t* k,
+                    const uint16_t* vt, const uint16_t* dout, const float* lse,
+                    const float* delta, uint8_t* ws, float* dk, float* dvt,
+                    cudaStream_t stream);
+int launch_bwd_queries(const Dims& d, const DevCtx& ctx, const uint16_t* k, const uint8_t* ws,
+                       float* dq, cudaStream_t stream);
+int launch_wait_probe(const DevCtx& ctx, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace css

@@ -1,0 +1,202 @@
+// bwd_queries.cu - the dQ pass: one 128-query tile of one query head per
+// CTA, dQ = s * sum over the visible key tiles of dS K, dS read back from the
+// workspace the key pass filled.
+//
+// Method (StreamingAttentionSM86.alpha, streamingAttentionQueryFromScores
+// section and the page-1 header of the split backward): for each key tile up
+// to the diagonal, dQ += dS K with dS taken from the stored dS^T read
+// transposed; the epilogue scales by s and stores binary32 rows.
+//
+// GB300 design: warp 4 copies each workspace tile (32 KiB, already in the
+// shared-memory image the tensor core reads) with one bulk copy and K's tile
+// with TMA, through a 4-stage ring; warp 5 issues dQ += dS K with dS as an
+// MN-major A operand (queries along the 128-byte rows) and K as an MN-major
+// B operand; warps 0-3 scale and store.  The pass is bound by reading dS
+// from HBM.
+#include <math.h>
+
+#include <mutex>
+
+#include "attn_internal.h"
+#include "sm103.cuh"
+
+namespace css {
+namespace {
+
+constexpr int kBM = 128;  // queries per CTA
+constexpr int kBN = 128;  // keys per tile
+constexpr int kThreads = 192;
+constexpr int kStages = 4;
+constexpr uint32_t kKTileBytes = 16384;
+constexpr uint32_t kStageBytes = kDsTileBytes + kKTileBytes;  // dS^T image, then K tile
+constexpr uint32_t kSmemBar = kStages * kStageBytes;
+constexpr uint32_t kSmemBytes = kSmemBar + 128 + 1024;
+constexpr uint32_t kTmemCols = 64;
+constexpr uint32_t kIdesc = idesc_f16_f32(128, 64, 1, 1);  // dS (MN-major) x K (MN-major)
+
+enum { BAR_FULL = 0, BAR_EMPTY = kStages, BAR_DONE = 2 * kStages, BAR_COUNT };
+static_assert(BAR_COUNT * 8 <= 128, "barrier area");
+
+struct QueriesArgs {
+  Dims d;
+  const uint8_t* ws;
+  float* dq;
+  uint32_t* err;
+  uint64_t wait_ns;
+};
+
+__device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
+
+static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_queries_kernel(const __grid_constant__ CUtensorMap tm_k, const QueriesArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t bar0 = sbase + kSmemBar;
+#define BAR(i) (bar0 + 8u * (uint32_t)(i))
+
+  const Dims& d = a.d;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h_local = blockIdx.x;
+  const int h = d.kv_begin * d.G + h_local;
+  const int kv = h / d.G;
+  const int it = (int)gridDim.y - 1 - (int)blockIdx.y;  // heaviest causal tiles first
+  const int b = blockIdx.z;
+  const int T = d.T;
+  int len = T;
+  if (d.lens) {
+    len = d.lens[b];
+    len = len < 0 ? 0 : (len > T ? T : len);
+  }
+  const int q0 = it * kBM;
+  int n_kt = 0;
+  if (q0 < len) n_kt = d.causal ? it + 1 : (len + kBN - 1) / kBN;
+  const int Hc = d.kv_count * d.G;
+  const long long tile0 = ((long long)b * Hc + h_local) * d.npairs;
+
+  WaitCtl wc{a.err, a.wait_ns, &s_abort};
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(BAR(BAR_FULL + s), 1);
+      mbar_init(BAR(BAR_EMPTY + s), 1);
+    }
+    mbar_init(BAR(BAR_DONE), 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 5) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 4) {
+    // ---------------- producer: workspace tile (bulk) + K tile (TMA) ----------------
+    if (lane == 0 && n_kt > 0) {
+      tma_prefetch_desc(&tm_k);
+      const int kvplane = b * d.Hkv + kv;
+      int issued = 0;
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages && !mbar_wait(BAR(BAR_EMPTY + s), ((j / kStages) - 1) & 1, wc)) break;
+        const uint32_t st = sbase + s * kStageBytes;
+        mbar_arrive_expect_tx(BAR(BAR_FULL + s), kStageBytes);
+        bulk_load(st, a.ws + (size_t)(tile0 + d.pair(it, j)) * kDsTileBytes, kDsTileBytes,
+                  BAR(BAR_FULL + s));
+        tma_load_3d(st + kDsTileBytes, &tm_k, BAR(BAR_FULL + s), 0, j * kBN, kvplane);
+        issued = j + 1;
+      }
+      for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
+        drain_wait(BAR(BAR_FULL + j % kStages), (j / kStages) & 1, a.wait_ns);
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && n_kt > 0) {
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j % kStages;
+        if (!mbar_wait(BAR(BAR_FULL + s), (j / kStages) & 1, wc)) break;
+        tc_fence_after();
+        const uint32_t ds_s = sbase + s * kStageBytes;
+        const uint32_t k_s = ds_s + kDsTileBytes;
+        // reduction over the tile's 128 keys, 16 rows (2 KiB) per step, in
+        // both operands; dS's two 64-query blocks are 16 KiB apart
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem, sdesc_sw128(ds_s + kk * 2048, 16384, 1024),
+                 sdesc_sw128(k_s + kk * 2048, 8192, 1024), kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(BAR(BAR_EMPTY + s));
+      }
+      mma_commit(BAR(BAR_DONE));
+    }
+  } else {
+    // ---------------- epilogue: dQ = s * sum ----------------
+    const int q = q0 + threadIdx.x;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float* dqrow = a.dq + (((size_t)b * d.H + h) * T + q) * 64;
+    if (n_kt > 0) {
+      mbar_wait(BAR(BAR_DONE), 0, wc);
+      tc_fence_after();
+      uint32_t r0[32], r1[32];
+      tmem_ld32x2_wait(tmem + lane_base, tmem + lane_base + 32, r0, r1);
+      if (q < T) {
+        float4* dst = reinterpret_cast<float4*>(dqrow);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          dst[u] = make_float4(as_f(r0[4 * u]) * d.scale, as_f(r0[4 * u + 1]) * d.scale,
+                               as_f(r0[4 * u + 2]) * d.scale, as_f(r0[4 * u + 3]) * d.scale);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          dst[8 + u] = make_float4(as_f(r1[4 * u]) * d.scale, as_f(r1[4 * u + 1]) * d.scale,
+                                   as_f(r1[4 * u + 2]) * d.scale, as_f(r1[4 * u + 3]) * d.scale);
+      }
+    } else if (q < T) {
+      float4* dst = reinterpret_cast<float4*>(dqrow);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) dst[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    if (n_kt > 0) drain_wait(BAR(BAR_DONE), 0, a.wait_ns);
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+#undef BAR
+}
+
+}  // namespace
+
+int launch_bwd_queries(const Dims& d, const DevCtx& ctx, const uint16_t* k, const uint8_t* ws,
+                       float* dq, cudaStream_t stream) {
+  CUtensorMap tk;
+  const uint64_t T = (uint64_t)d.T;
+  if (!encode_tmap_3d(&tk, k, 64, T, (uint64_t)d.B * d.Hkv, 128, T * 128, 64, kBN))
+    return ATTN_ERR_CUDA;
+  static std::once_flag attr_once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::call_once(attr_once[dev & 63], [] {
+    cudaFuncSetAttribute(bwd_queries_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kSmemBytes);
+  });
+  QueriesArgs args{d, ws, dq, ctx.err, ctx.wait_ns};
+  dim3 grid(d.kv_count * d.G, d.nt, d.B);
+  bwd_queries_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tk, args);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace css

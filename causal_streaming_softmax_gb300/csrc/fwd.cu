@@ -1,0 +1,358 @@
+// fwd.cu - forward pass: causal (or length-masked) attention as a streaming
+// normalised sum, one 128-query tile of one query head per CTA.
+//
+// Method (StreamingAttentionSM86.alpha, forward module header and the
+// "one key tile" / epilogue sections): for every key tile up to the
+// diagonal, S = Q K^T; t = S c in base 2; m' = max(m, rowmax t);
+// alpha = 2^(m - m'); P = 2^(t - m'); l = alpha l + sum P (binary32, P
+// unrounded); O = alpha O + f16(P) V.  Output O / l (binary16, token-major)
+// and L = m + log2 l (binary32).
+//
+// GB300 design (not the pages' SM86 register kernel): warp-specialised CTA
+//   warps 0-3  softmax: one thread per query row (= tensor-memory lane)
+//   warp 4     TMA producer: Q once, then K / V^T tiles through a 2-stage ring
+//   warp 5     MMA issuer: S = Q K^T (SS) and O += P V (P from tensor memory)
+// Tensor memory: S 128 columns (binary32), P 64 columns (binary16 pairs),
+// O 64 columns (binary32): 256 columns, so two CTAs share an SM and one CTA's
+// softmax overlaps the other's MMAs.
+#include <math.h>
+
+#include <mutex>
+
+#include "attn_internal.h"
+#include "sm103.cuh"
+
+namespace css {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr uint32_t kQTileBytes = 128 * 128;        // 128 rows x 128 B
+constexpr uint32_t kStageBytes = 2 * kQTileBytes;  // K tile, then V^T as two 64-key halves
+constexpr uint32_t kSmemQ = 0;
+constexpr uint32_t kSmemStage0 = kQTileBytes;
+constexpr uint32_t kSmemBar = kSmemStage0 + kStages * kStageBytes;
+constexpr uint32_t kSmemBytes = kSmemBar + 128 + 1024;  // barriers + 1024-B alignment slack
+
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColP = 128;
+constexpr uint32_t kColO = 192;
+constexpr uint32_t kTmemCols = 256;
+
+constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);  // Q (K-major) x K (K-major)
+constexpr uint32_t kIdescO = idesc_f16_f32(128, 64, 0, 0);   // P (tmem) x V^T (K-major)
+
+enum {
+  BAR_Q = 0,
+  BAR_KV_FULL = 1,
+  BAR_KV_EMPTY = BAR_KV_FULL + kStages,
+  BAR_S_FULL = BAR_KV_EMPTY + kStages,
+  BAR_P_FULL,
+  BAR_O_DONE,
+  BAR_COUNT
+};
+static_assert(BAR_COUNT * 8 <= 128, "barrier area");
+
+struct FwdArgs {
+  int T, H, Hkv, G, causal;
+  const int32_t* lens;
+  float c;
+  uint16_t* o;
+  float* lse;
+  uint32_t* err;
+  uint64_t wait_ns;
+};
+
+__device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
+
+// Waits used only to drain in-flight asynchronous work before the CTA exits
+// (they ignore the abort flag; bounded by the same limit).
+static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_vt, const FwdArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t bar0 = sbase + kSmemBar;
+#define BAR(i) (bar0 + 8u * (uint32_t)(i))
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.x;
+  const int qt = (int)gridDim.y - 1 - (int)blockIdx.y;  // heaviest causal tiles first
+  const int b = blockIdx.z;
+  const int kv = h / a.G;
+  const int T = a.T;
+  int len = T;
+  if (a.lens) {
+    len = a.lens[b];
+    len = len < 0 ? 0 : (len > T ? T : len);
+  }
+  const int q0 = qt * kBM;
+  int n_kt = 0;
+  if (q0 < len) {
+    const int kend = a.causal ? min(len, q0 + kBM) : len;
+    n_kt = (kend + kBN - 1) / kBN;
+  }
+
+  WaitCtl wc{a.err, a.wait_ns, &s_abort};
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    mbar_init(BAR(BAR_Q), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(BAR(BAR_KV_FULL + s), 1);
+      mbar_init(BAR(BAR_KV_EMPTY + s), 1);
+    }
+    mbar_init(BAR(BAR_S_FULL), 1);
+    mbar_init(BAR(BAR_P_FULL), 128);
+    mbar_init(BAR(BAR_O_DONE), 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 5) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0 && n_kt > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_vt);
+      const int qplane = b * a.H + h;
+      const int kvplane = b * a.Hkv + kv;
+      mbar_arrive_expect_tx(BAR(BAR_Q), kQTileBytes);
+      tma_load_3d(sbase + kSmemQ, &tm_q, BAR(BAR_Q), 0, q0, qplane);
+      int issued = 0;
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages && !mbar_wait(BAR(BAR_KV_EMPTY + s), ((j / kStages) - 1) & 1, wc)) break;
+        const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
+        mbar_arrive_expect_tx(BAR(BAR_KV_FULL + s), kStageBytes);
+        tma_load_3d(st, &tm_k, BAR(BAR_KV_FULL + s), 0, j * kBN, kvplane);
+        tma_load_3d(st + kQTileBytes, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN, 0, kvplane);
+        tma_load_3d(st + kQTileBytes + 8192, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN + 64, 0,
+                    kvplane);
+        issued = j + 1;
+      }
+      // No copy may still be landing when the CTA exits (matters only when a
+      // wait gave up): wait for the last fill of each stage and for Q.
+      drain_wait(BAR(BAR_Q), 0, a.wait_ns);
+      for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
+        drain_wait(BAR(BAR_KV_FULL + j % kStages), (j / kStages) & 1, a.wait_ns);
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer (one thread) ----------------
+    if (lane == 0 && n_kt > 0) {
+      const uint32_t q_s = sbase + kSmemQ;
+      bool ok = mbar_wait(BAR(BAR_Q), 0, wc);
+      for (int j = 0; ok && j < n_kt; ++j) {
+        const int s = j % kStages;
+        if (!mbar_wait(BAR(BAR_KV_FULL + s), (j / kStages) & 1, wc)) break;
+        tc_fence_after();
+        const uint32_t k_s = sbase + kSmemStage0 + s * kStageBytes;
+        const uint32_t v_s = k_s + kQTileBytes;
+        // S = Q K^T over d = 64: four K=16 steps inside the 128-byte atom.
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tmem + kColS, sdesc_sw128(q_s + kk * 32, 16, 1024),
+                 sdesc_sw128(k_s + kk * 32, 16, 1024), kIdescS, kk > 0);
+        mma_commit(BAR(BAR_S_FULL));
+        if (!mbar_wait(BAR(BAR_P_FULL), j & 1, wc)) break;
+        tc_fence_after();
+        // O += P V over the tile's 128 keys: eight K=16 steps; keys 0-63 in
+        // the first V^T half, 64-127 in the second.
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + kColO, tmem + kColP + kk * 8,
+                 sdesc_sw128(v_s + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), kIdescO,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(BAR(BAR_KV_EMPTY + s));
+      }
+      mma_commit(BAR(BAR_O_DONE));
+    }
+  } else {
+    // ---------------- softmax: thread = query row ----------------
+    const int row = threadIdx.x;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + kColS;
+    const uint32_t t_p = tmem + lane_base + kColP;
+    const uint32_t t_o = tmem + lane_base + kColO;
+    const int qrow = q0 + row;
+    const bool row_ok = qrow < len;
+    // keys below `lim` are valid for this row
+    int lim = row_ok ? len : 0;
+    if (a.causal) lim = min(lim, qrow + 1);
+    const float c = a.c;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kt; ++j) {
+      if (!mbar_wait(BAR(BAR_S_FULL), j & 1, wc)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int k0 = j * kBN;
+      const bool need_mask =
+          (a.causal && k0 + kBN - 1 > q0) || (k0 + kBN > len) || (q0 + kBM > len);
+      const int lim_local = lim - k0;
+
+      // pass 1: the row's maximum raw score over the tile
+      float mx = -INFINITY;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32x2_wait(t_s + half * 64, t_s + half * 64 + 32, v0, v1);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float x0 = as_f(v0[e]), x1 = as_f(v1[e]);
+          if (need_mask) {
+            if (half * 64 + e >= lim_local) x0 = -INFINITY;
+            if (half * 64 + 32 + e >= lim_local) x1 = -INFINITY;
+          }
+          mx = fmaxf(mx, fmaxf(x0, x1));
+        }
+      }
+      // c > 0, so max(S) c is the maximum of the scaled scores.
+      const float m_new = fmaxf(m, mx * c);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2_approx(m - m_use);
+      const float neg_m = -m_use;
+
+      // pass 2: P = 2^(S c - m'), the row sum, and P as binary16 into tensor memory
+      float sum = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32x2_wait(t_s + half * 64, t_s + half * 64 + 32, v0, v1);
+        uint32_t p0[16], p1[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float x0 = as_f(v0[e]), x1 = as_f(v0[e + 1]);
+          float y0 = as_f(v1[e]), y1 = as_f(v1[e + 1]);
+          if (need_mask) {
+            const int cb = half * 64 + e;
+            if (cb >= lim_local) x0 = -INFINITY;
+            if (cb + 1 >= lim_local) x1 = -INFINITY;
+            if (cb + 32 >= lim_local) y0 = -INFINITY;
+            if (cb + 33 >= lim_local) y1 = -INFINITY;
+          }
+          const float e0 = ex2_approx(fmaf(x0, c, neg_m));
+          const float e1 = ex2_approx(fmaf(x1, c, neg_m));
+          const float f0 = ex2_approx(fmaf(y0, c, neg_m));
+          const float f1 = ex2_approx(fmaf(y1, c, neg_m));
+          sum += (e0 + e1) + (f0 + f1);
+          p0[e >> 1] = pack_f16x2(e0, e1);
+          p1[e >> 1] = pack_f16x2(f0, f1);
+        }
+        tmem_st16(t_p + half * 32, p0);
+        tmem_st16(t_p + half * 32 + 16, p1);
+      }
+      l = l * alpha + sum;
+      m = m_new;
+
+      // O *= alpha (the previous tile's P V has completed: this tile's S,
+      // committed after it, has).  Skipped for a warp whose rows all keep
+      // their maximum, which leaves O unchanged exactly.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        uint32_t o0[32], o1[32];
+        tmem_ld32x2_wait(t_o, t_o + 32, o0, o1);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          o0[e] = __float_as_uint(as_f(o0[e]) * alpha);
+          o1[e] = __float_as_uint(as_f(o1[e]) * alpha);
+        }
+        tmem_st32(t_o, o0);
+        tmem_st32(t_o + 32, o1);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(BAR(BAR_P_FULL));
+    }
+
+    // ---------------- epilogue: O / l, L = m + log2 l ----------------
+    uint16_t* orow = a.o + ((size_t)((size_t)b * T + qrow) * a.H + h) * 64;
+    float* lrow = a.lse + ((size_t)b * a.H + h) * T + qrow;
+    if (n_kt > 0) {
+      ok = ok && mbar_wait(BAR(BAR_O_DONE), 0, wc);
+      tc_fence_after();
+      uint32_t o0[32], o1[32];
+      tmem_ld32x2_wait(t_o, t_o + 32, o0, o1);
+      const bool valid = row_ok && l > 0.f;
+      const float inv = valid ? 1.0f / l : 0.f;
+      if (qrow < T) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          dst[u] = make_uint4(pack_f16x2(as_f(o0[8 * u + 0]) * inv, as_f(o0[8 * u + 1]) * inv),
+                              pack_f16x2(as_f(o0[8 * u + 2]) * inv, as_f(o0[8 * u + 3]) * inv),
+                              pack_f16x2(as_f(o0[8 * u + 4]) * inv, as_f(o0[8 * u + 5]) * inv),
+                              pack_f16x2(as_f(o0[8 * u + 6]) * inv, as_f(o0[8 * u + 7]) * inv));
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          dst[4 + u] =
+              make_uint4(pack_f16x2(as_f(o1[8 * u + 0]) * inv, as_f(o1[8 * u + 1]) * inv),
+                         pack_f16x2(as_f(o1[8 * u + 2]) * inv, as_f(o1[8 * u + 3]) * inv),
+                         pack_f16x2(as_f(o1[8 * u + 4]) * inv, as_f(o1[8 * u + 5]) * inv),
+                         pack_f16x2(as_f(o1[8 * u + 6]) * inv, as_f(o1[8 * u + 7]) * inv));
+        *lrow = valid ? m + lg2_approx(l) : -INFINITY;
+      }
+    } else if (qrow < T) {
+      uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) dst[u] = make_uint4(0, 0, 0, 0);
+      *lrow = -INFINITY;
+    }
+    (void)ok;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    // every MMA of this CTA has completed before its tensor memory is freed
+    if (n_kt > 0) drain_wait(BAR(BAR_O_DONE), 0, a.wait_ns);
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+#undef BAR
+}
+
+}  // namespace
+
+int launch_fwd(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16_t* k,
+               const uint16_t* vt, uint16_t* o, float* lse, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  const uint64_t T = (uint64_t)d.T;
+  // Q [B*H][T][64], K [B*Hkv][T][64]: boxes of 128 rows x 64 values.
+  if (!encode_tmap_3d(&tq, q, 64, T, (uint64_t)d.B * d.H, 128, T * 128, 64, kBM) ||
+      !encode_tmap_3d(&tk, k, 64, T, (uint64_t)d.B * d.Hkv, 128, T * 128, 64, kBN) ||
+      // V^T [B*Hkv][64][T]: boxes of 64 keys x 64 rows.
+      !encode_tmap_3d(&tv, vt, T, 64, (uint64_t)d.B * d.Hkv, T * 2, T * 128, 64, 64))
+    return ATTN_ERR_CUDA;
+  static std::once_flag attr_once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::call_once(attr_once[dev & 63], [] {
+    cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  FwdArgs args{d.T, d.H, d.Hkv, d.G, d.causal, d.lens, d.c, o, lse, ctx.err, ctx.wait_ns};
+  dim3 grid(d.H, d.nt, d.B);
+  fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, args);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace css

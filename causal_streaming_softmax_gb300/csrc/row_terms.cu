@@ -1,0 +1,105 @@
+// row_terms.cu - D = rowsum(dO * O) per query row, and the bounded-wait probe.
+//
+// Method: streamingAttentionRowTermsOrderedUncheckedSM86 (page 1 header and
+// definition): the backward pass's row terms, D_i = sum_d dO_id O_id from the
+// stored binary16 O and dO, summed in binary32, written [head][T].  Rows at
+// or past a sequence's length get D = 0.
+//
+// Memory-bound: eight threads share a row, each reading 16 bytes of dO (row
+// r of [B][H][T][64]) and 16 bytes of O (token-major [B][T][H*64]); a
+// three-step butterfly inside the eight-lane group forms the sum.
+#include <math.h>
+
+#include "attn_internal.h"
+#include "sm103.cuh"
+
+namespace css {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float dot8(uint4 a, uint4 b) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    acc = fmaf(f16_bits_to_f32((uint16_t)(aw[u] & 0xFFFFu)),
+               f16_bits_to_f32((uint16_t)(bw[u] & 0xFFFFu)), acc);
+    acc = fmaf(f16_bits_to_f32((uint16_t)(aw[u] >> 16)), f16_bits_to_f32((uint16_t)(bw[u] >> 16)),
+               acc);
+  }
+  return acc;
+}
+
+__global__ void __launch_bounds__(kThreads)
+    row_terms_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                     float* __restrict__ delta, int B, int T, int H,
+                     const int32_t* __restrict__ lens) {
+  const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
+  const long long row = gid >> 3;  // (b * H + h) * T + t
+  const int part = threadIdx.x & 7;
+  const long long nrows = (long long)B * H * T;
+  const bool active = row < nrows;
+  float acc = 0.f;
+  int t = 0, b = 0;
+  if (active) {
+    t = (int)(row % T);
+    const long long bh = row / T;
+    const int h = (int)(bh % H);
+    b = (int)(bh / H);
+    const uint4 dv = __ldg(reinterpret_cast<const uint4*>(dout + row * 64) + part);
+    const uint4 ov = __ldg(
+        reinterpret_cast<const uint4*>(o + (((long long)b * T + t) * H + h) * 64) + part);
+    acc = dot8(dv, ov);
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  if (active && part == 0) {
+    int len = T;
+    if (lens) {
+      len = lens[b];
+      len = len < 0 ? 0 : (len > T ? T : len);
+    }
+    delta[row] = t < len ? acc : 0.f;
+  }
+}
+
+// One block waits on a barrier that nothing completes, with a short limit:
+// the wait must give up, record the timeout and let the kernel return.
+__global__ void wait_probe_kernel(uint32_t* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    WaitCtl w{err, limit_ns, &abort_flag};
+    (void)mbar_wait(smem_u32(&bar), 0, w);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+int launch_row_terms(const Dims& d, const DevCtx& ctx, const uint16_t* o, const uint16_t* dout,
+                     float* delta, cudaStream_t stream) {
+  (void)ctx;
+  const long long threads = (long long)d.B * d.H * d.T * 8;
+  const long long blocks = (threads + kThreads - 1) / kThreads;
+  if (blocks > 0x7FFFFFFFll) return ATTN_ERR_SHAPE;
+  row_terms_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(o, dout, delta, d.B, d.T, d.H,
+                                                               d.lens);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int launch_wait_probe(const DevCtx& ctx, uint64_t limit_ns, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(ctx.err, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace css

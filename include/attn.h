@@ -1,0 +1,187 @@
+/*
+ * attn.h - C ABI of the GB300 (sm_103a) causal streaming-softmax attention
+ * library, libattn.so.
+ *
+ * The method (StreamingAttentionSM86.alpha, lsalpha source view):
+ *   forward   module header: for every 64-key block the running base-2 row
+ *             maximum m, row sum l and fp32 weighted sum O are rescaled by
+ *             2^(m - m') and the block's P V added; O / l is the output and
+ *             L = m + log2 l the base-2 log-sum-exp.  Scores are taken in
+ *             base 2 as t = S c, c = fp32-nearest(scale / ln 2); P is rounded
+ *             to binary16 before its product with V; sums stay binary32.
+ *   backward  header of the backward pass: P = 2^(S c - L), dP = dO V^T,
+ *             D = rowsum(dO * O), dS = P (dP - D), dQ = s dS K,
+ *             dK = s dS^T Q, dV = P^T dO (s = the natural scale), with no
+ *             atomics (deterministic), split as the page-1 header of
+ *             streamingAttentionRowTermsOrderedUncheckedSM86 describes: row
+ *             terms, then a key pass that stores dS, then dQ from stored dS.
+ *   lengths   gist self_attn_fwd (snippet.py): query rows and keys at or past
+ *             a sequence's length are masked; such rows output zero.
+ *
+ * Layouts (the pages' planes with a leading batch index added), all dense
+ * row-major, element sizes in brackets:
+ *   q, dout   [B][H][T][64]      binary16 (uint16_t bit patterns)
+ *   k         [B][Hkv][T][64]    binary16
+ *   vt        [B][Hkv][64][T]    binary16 (V transposed)
+ *   o         [B][T][H*64]       binary16 (token-major, heads merged)
+ *   lse,delta [B][H][T]          binary32 (lse in base 2)
+ *   dq        [B][H][T][64]      binary32
+ *   dk        [B][Hkv][T][64]    binary32 (summed over each K/V head's group)
+ *   dvt       [B][Hkv][64][T]    binary32 (dV transposed, unscaled)
+ * Query head h reads K/V head h / (H / Hkv).
+ *
+ * Ownership: the caller allocates every buffer (device memory) and the
+ * backward workspace; the library allocates no device memory (only tensor
+ * memory inside its kernels) and keeps no state beyond cached per-device
+ * properties.  Every call is asynchronous on the given stream (a
+ * cudaStream_t passed as void*; NULL is the legacy default stream) and
+ * returns after the launch.
+ *
+ * Errors: every entry point validates its arguments on the host before any
+ * launch and returns one of the ATTN_ codes below; nothing is launched when
+ * the result is not ATTN_OK.  Device-side failures (a bounded wait that ran
+ * out) are reported by attn_last_device_error.
+ */
+#ifndef CSS_ATTN_H
+#define CSS_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  ATTN_OK = 0,
+  ATTN_ERR_SHAPE = -1,          /* shape outside the admission rules below   */
+  ATTN_ERR_NULL = -2,           /* a required pointer is NULL                */
+  ATTN_ERR_ALIGN = -3,          /* a buffer is not 16-byte aligned           */
+  ATTN_ERR_WORKSPACE = -4,      /* workspace smaller than required           */
+  ATTN_ERR_CUDA = -5,           /* a CUDA runtime/driver call failed         */
+  ATTN_ERR_DEVICE_TIMEOUT = -6, /* a kernel's bounded wait ran out           */
+  ATTN_ERR_DEVICE = -7          /* the current device is not sm_103          */
+};
+
+/*
+ * Problem shape.  Admission (the pages' admission predicate, "the program"
+ * section of StreamingAttentionSM86.alpha): seq > 0 and a multiple of 64,
+ * heads a multiple of kv_heads, heads <= 65535, head_dim == 64.  batch >= 1.
+ * The pages' 32-bit byte-offset bound does not apply: offsets are 64-bit.
+ *
+ * seq_lens: NULL, or a DEVICE array [batch] of int32 lengths in 0..seq
+ *   (values outside are clamped).  Query rows i >= len give O = 0,
+ *   L = -inf, D = 0, dQ = 0; keys j >= len get dK = dV = 0.
+ * causal: 1 masks keys after the query (the diagonal is kept); 0 attends to
+ *   every key below the length.
+ * scale: the natural score scale s; the kernels use c = fp32(s / ln 2).
+ * head_begin, head_count: a chunk of K/V heads for attn_bwd_keys and
+ *   attn_bwd_queries (with all their query heads); 0, 0 means all.  The
+ *   workspace holds the chunk only, so a caller can bound it (or keep it
+ *   L2-resident) by walking the heads in chunks.  attn_fwd and
+ *   attn_row_terms ignore the chunk.
+ */
+typedef struct attn_shape {
+  int32_t batch;
+  int32_t seq;
+  int32_t heads;
+  int32_t kv_heads;
+  int32_t head_dim;
+  int32_t causal;
+  const int32_t* seq_lens;
+  float scale;
+  int32_t head_begin;
+  int32_t head_count;
+} attn_shape;
+
+/*
+ * Forward pass (forward module header; "one key tile" and epilogue
+ * sections).  Reads q, k, vt; writes o and lse.  All pointers device,
+ * 16-byte aligned.
+ */
+ATTN_API int attn_fwd(const attn_shape* shape, const uint16_t* q, const uint16_t* k,
+             const uint16_t* vt, uint16_t* o, float* lse, void* stream);
+
+/*
+ * Row terms D = rowsum(dO * O) (streamingAttentionRowTermsOrderedUncheckedSM86,
+ * page 1): the stored binary16 O and dO widened, summed in binary32.
+ * Reads o and dout; writes delta [B][H][T].  Device pointers, 16-byte aligned.
+ */
+ATTN_API int attn_row_terms(const attn_shape* shape, const uint16_t* o,
+                   const uint16_t* dout, float* delta, void* stream);
+
+/*
+ * Bytes of the dS workspace that attn_bwd_keys writes and attn_bwd_queries
+ * reads for this shape and head chunk (0 if the shape is invalid).  The
+ * layout inside is private to the library: per (batch, query head of the
+ * chunk, 128-query block, 128-key block) one 32 KiB binary16 tile of dS^T,
+ * causal shapes storing only blocks on or below the diagonal.
+ */
+ATTN_API size_t attn_bwd_workspace_bytes(const attn_shape* shape);
+
+/*
+ * Key pass (key launch of StreamingAttentionSM86.alpha, with the score
+ * gradients stored as the page-1 header describes).  For each 128-key block
+ * of each K/V head in the chunk and each query block that can see it:
+ * S^T = K Q^T, P^T = 2^(S^T c - L), dP^T = V dO^T, dS^T = P^T (dP^T - D);
+ * dV += P^T dO and dK += dS^T Q over every query head of the group; dS^T is
+ * stored (binary16) into ds_ws.  Writes dk = s * sum and dvt (unscaled) for
+ * the chunk's K/V heads.  Needs lse from attn_fwd and delta from
+ * attn_row_terms.  ds_ws: device, ws_bytes >= attn_bwd_workspace_bytes.
+ */
+ATTN_API int attn_bwd_keys(const attn_shape* shape, const uint16_t* q, const uint16_t* k,
+                  const uint16_t* vt, const uint16_t* dout, const float* lse,
+                  const float* delta, void* ds_ws, size_t ws_bytes, float* dk,
+                  float* dvt, void* stream);
+
+/*
+ * dQ pass (streamingAttentionQueryFromScores section): for each 128-query
+ * block, dQ = s * sum over visible key blocks of dS K, dS read from the
+ * workspace attn_bwd_keys filled for the same shape and chunk.  Writes dq
+ * for the chunk's query heads.
+ */
+ATTN_API int attn_bwd_queries(const attn_shape* shape, const uint16_t* k,
+                     const void* ds_ws, size_t ws_bytes, float* dq,
+                     void* stream);
+
+/* A static, human-readable message for an ATTN_ code. */
+ATTN_API const char* attn_error_string(int code);
+
+/*
+ * Synchronises the stream, then reports and clears the current device's
+ * device-side error word: ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT when a kernel
+ * gave up a bounded wait (its outputs are then undefined).  ATTN_ERR_CUDA if
+ * the synchronisation itself failed.
+ */
+ATTN_API int attn_last_device_error(void* stream);
+
+/*
+ * Sets the time limit of every bounded wait inside the kernels launched
+ * afterwards on any device (nanoseconds; 0 restores the default of 2 s).
+ * Not part of the method: a safety bound so that a kernel never spins
+ * forever.
+ */
+ATTN_API void attn_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * Self-test of the bounded wait: launches one block that waits on a barrier
+ * nothing will complete, with a limit of limit_ns, then synchronises and
+ * returns what attn_last_device_error reports (ATTN_ERR_DEVICE_TIMEOUT when
+ * the wait gave up as it should).  Not part of the method.
+ */
+ATTN_API int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+ATTN_API int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSS_ATTN_H */
