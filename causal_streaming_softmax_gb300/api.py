@@ -247,3 +247,52 @@ def forward_backward(s: Shape, q, k, vt, dout, bufs: Buffers, stream=None) -> Bu
     attn_bwd_keys(s, q, k, vt, dout, bufs.lse, bufs.delta, bufs.ws, bufs.dk, bufs.dvt, stream)
     attn_bwd_queries(s, k, bufs.ws, bufs.dq, stream)
     return bufs
+
+
+class HostProblem:
+    """Pinned host copies of one problem's inputs and outputs, for callers
+    whose data lives in host memory."""
+
+    def __init__(self, s: Shape, q, k, vt, dout):
+        B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
+        pin = lambda t: t.contiguous().pin_memory()
+        self.q, self.k, self.vt, self.dout = pin(q), pin(k), pin(vt), pin(dout)
+        e = lambda shape, dt: torch.empty(shape, dtype=dt).pin_memory()
+        self.o = e((B, T, H * 64), torch.float16)
+        self.lse = e((B, H, T), torch.float32)
+        self.dq = e((B, H, T, 64), torch.float32)
+        self.dk = e((B, Hkv, T, 64), torch.float32)
+        self.dvt = e((B, Hkv, 64, T), torch.float32)
+
+    def input_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.q, self.k, self.vt, self.dout))
+
+    def output_bytes(self) -> int:
+        return sum(t.numel() * t.element_size()
+                   for t in (self.o, self.lse, self.dq, self.dk, self.dvt))
+
+
+class DeviceInputs:
+    def __init__(self, s: Shape, device=None):
+        dev = device or torch.device("cuda")
+        B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
+        self.q = torch.empty((B, H, T, 64), dtype=torch.float16, device=dev)
+        self.k = torch.empty((B, Hkv, T, 64), dtype=torch.float16, device=dev)
+        self.vt = torch.empty((B, Hkv, 64, T), dtype=torch.float16, device=dev)
+        self.dout = torch.empty((B, H, T, 64), dtype=torch.float16, device=dev)
+
+
+def forward_backward_host(s: Shape, host: HostProblem, dev_in: DeviceInputs, bufs: Buffers,
+                          stream=None) -> None:
+    """Host-to-host pass on one stream: copy the inputs in, run the four
+    calls, copy O, L, dQ, dK and dV^T back (asynchronous; synchronise the
+    stream before reading ``host``'s outputs)."""
+    st = stream if stream is not None else torch.cuda.current_stream()
+    with torch.cuda.stream(st):
+        for dst, src in ((dev_in.q, host.q), (dev_in.k, host.k), (dev_in.vt, host.vt),
+                         (dev_in.dout, host.dout)):
+            dst.copy_(src, non_blocking=True)
+        forward_backward(s, dev_in.q, dev_in.k, dev_in.vt, dev_in.dout, bufs, st)
+        for dst, src in ((host.o, bufs.o), (host.lse, bufs.lse), (host.dq, bufs.dq),
+                         (host.dk, bufs.dk), (host.dvt, bufs.dvt)):
+            dst.copy_(src, non_blocking=True)

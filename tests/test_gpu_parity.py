@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Small shapes are compared element by element over the whole problem (they
+span several 128-row tiles and ragged tails); the full-size workloads are
+compared on sampled rows and keys that the oracle computes one by one, in
+the same launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from causal_streaming_softmax_gb300 import workloads
+from parity_util import GRAD_TOL, L_TOL, O_TOL, compare_full, rel_fro, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _full(inp, causal, scale=0.125):
+    return oracle.backward(inp["q"], inp["k"], inp["vt"], inp["dout"], causal=causal,
+                           scale=scale, lens=inp["lens"])
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_workload_full(cuda_device, cfg):
+    w = workloads.WORKLOADS[cfg]
+    inp = workloads.make_inputs(w)
+    gpu = run_gpu(inp, causal=w.causal, scale=w.scale)
+    compare_full(gpu, _full(inp, w.causal, w.scale), inp)
+
+
+EDGE = [
+    # B, T, H, Hkv, causal, lens
+    (1, 64, 1, 1, True, None),          # one 64-row block: half of a 128 tile
+    (1, 192, 4, 2, True, None),         # ragged tail
+    (1, 320, 8, 1, True, None),         # group 8, several tiles + ragged tail
+    (2, 256, 4, 4, False, [1, 256]),    # length 1 and full, non-causal
+    (4, 256, 2, 1, False, [63, 64, 65, 200]),
+    (3, 384, 4, 2, True, [1, 129, 384]),  # causal with lengths
+    (2, 512, 2, 2, True, None),
+]
+
+
+@pytest.mark.parametrize("B,T,H,Hkv,causal,lens", EDGE)
+def test_edge_shapes(cuda_device, B, T, H, Hkv, causal, lens):
+    inp = workloads.make_custom_inputs(B, T, H, Hkv, causal=causal, lens=lens, seed=T + H)
+    gpu = run_gpu(inp, causal=causal)
+    compare_full(gpu, _full(inp, causal), inp)
+
+
+def test_sharp_softmax_small(cuda_device):
+    """Q ~ N(0, 16) as in the GQA workload, small enough for the full oracle."""
+    inp = workloads.make_custom_inputs(1, 512, 8, 2, causal=True, q_std=4.0, seed=33)
+    gpu = run_gpu(inp, causal=True)
+    compare_full(gpu, _full(inp, True), inp)
+
+
+def test_other_scale(cuda_device):
+    inp = workloads.make_custom_inputs(1, 256, 2, 1, causal=True, seed=5)
+    gpu = run_gpu(inp, causal=True, scale=0.3)
+    compare_full(gpu, _full(inp, True, 0.3), inp)
+
+
+def test_deterministic(cuda_device):
+    w = workloads.WORKLOADS[2]
+    inp = workloads.make_inputs(w)
+    a = run_gpu(inp, causal=True)
+    b = run_gpu(inp, causal=True)
+    for key in a:
+        assert np.array_equal(a[key], b[key], equal_nan=True), key
+
+
+def test_head_chunks_match_whole(cuda_device):
+    """The backward walked in K/V-head chunks (workspace per chunk) gives the
+    same bits as one call over every head."""
+    import torch
+    from causal_streaming_softmax_gb300 import api
+    inp = workloads.make_custom_inputs(1, 384, 8, 4, causal=True, seed=9)
+    whole = run_gpu(inp, causal=True)
+    dev = "cuda"
+    q, k, vt, dout = (torch.from_numpy(inp[n]).to(dev) for n in ("q", "k", "vt", "dout"))
+    s = api.Shape(1, 384, 8, 4, causal=True)
+    bufs = api.Buffers(s)
+    api.attn_fwd(s, q, k, vt, bufs.o, bufs.lse)
+    api.attn_row_terms(s, bufs.o, dout, bufs.delta)
+    for begin, count in ((0, 1), (1, 2), (3, 1)):
+        c = s.chunk(begin, count)
+        ws = api.alloc_workspace(c)
+        assert ws.numel() == api.workspace_bytes(s) * count // 4
+        api.attn_bwd_keys(c, q, k, vt, dout, bufs.lse, bufs.delta, ws, bufs.dk, bufs.dvt)
+        api.attn_bwd_queries(c, k, ws, bufs.dq)
+    torch.cuda.synchronize()
+    assert api.last_device_error() == 0
+    for name in ("dq", "dk", "dvt"):
+        assert np.array_equal(getattr(bufs, name).cpu().numpy(), whole[name]), name
+
+
+def test_wait_timeout_selftest(cuda_device):
+    """A bounded wait that nothing completes gives up, reports the timeout, and
+    the context stays usable."""
+    from causal_streaming_softmax_gb300 import api
+    assert api.selftest_wait_timeout(1_000_000) == api.ATTN_ERR_DEVICE_TIMEOUT
+    assert api.last_device_error() == 0  # reported once, then cleared
+    inp = workloads.make_inputs(workloads.WORKLOADS[1])
+    gpu = run_gpu(inp, causal=True)
+    compare_full(gpu, _full(inp, True), inp)
+
+
+def test_workspace_too_small_is_rejected(cuda_device):
+    import torch
+    from causal_streaming_softmax_gb300 import api
+    s = api.Shape(1, 256, 2, 1)
+    t = lambda *shape, dt=torch.float16: torch.zeros(shape, dtype=dt, device="cuda")
+    ws = torch.empty(api.workspace_bytes(s) - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(api.AttnError) as e:
+        api.attn_bwd_keys(s, t(1, 2, 256, 64), t(1, 1, 256, 64), t(1, 1, 64, 256),
+                          t(1, 2, 256, 64), t(1, 2, 256, dt=torch.float32),
+                          t(1, 2, 256, dt=torch.float32), ws, t(1, 1, 256, 64, dt=torch.float32),
+                          t(1, 1, 64, 256, dt=torch.float32))
+    assert e.value.code == api.ATTN_ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, compared on samples the oracle computes one by one
+# ---------------------------------------------------------------------------
+def _sample_rows(T, lens_b, rng, n=40):
+    cand = {0, 1, 63, 64, 127, 128, 129, T - 1, T - 2}
+    if lens_b is not None:
+        cand |= {lens_b - 1, lens_b, min(lens_b + 1, T - 1)}
+    cand |= set(rng.integers(0, T, size=n).tolist())
+    return np.array(sorted(r for r in cand if 0 <= r < T), dtype=np.int32)
+
+
+def _check_sampled(w, inp, gpu, heads, kv_heads, batches, rng):
+    B, H, T, d = inp["q"].shape
+    lens = inp["lens"]
+    worst = dict(o=0.0, l=0.0)
+    dq_num = dq_den = dk_num = dk_den = dv_num = dv_den = 0.0
+    o4 = gpu["o"].astype(np.float64).reshape(B, T, H, d)
+    for b in batches:
+        lb = None if lens is None else int(lens[b])
+        rows = _sample_rows(T, lb, rng)
+        for h in heads:
+            r = oracle.query_rows(inp["q"], inp["k"], inp["vt"], inp["dout"], b, h, rows,
+                                  causal=w.causal, scale=w.scale, lens=lens)
+            valid = rows < (T if lb is None else lb)
+            og = o4[b, rows, h]
+            assert np.all(og[~valid] == 0.0)
+            assert np.all(np.isneginf(gpu["lse"][b, h, rows[~valid]]))
+            if valid.any():
+                worst["o"] = max(worst["o"], float(np.max(np.abs(og[valid] - r["o"][valid]))))
+                worst["l"] = max(worst["l"], float(np.max(np.abs(
+                    gpu["lse"][b, h, rows[valid]] - r["lse"][valid]))))
+                dabs = np.abs(inp["dout"][b, h, rows[valid]].astype(np.float64)).sum(-1)
+                assert np.all(np.abs(gpu["delta"][b, h, rows[valid]] - r["delta"][valid])
+                              <= O_TOL * dabs + 1e-5)
+            dq_num += float(np.sum((gpu["dq"][b, h, rows] - r["dq"]) ** 2))
+            dq_den += float(np.sum(r["dq"] ** 2))
+        for kv in kv_heads:
+            keys = _sample_rows(T, lb, rng, n=24)
+            r = oracle.key_rows(inp["q"], inp["k"], inp["vt"], inp["dout"], b, kv, keys,
+                                causal=w.causal, scale=w.scale, lens=lens)
+            dk_num += float(np.sum((gpu["dk"][b, kv, keys] - r["dk"]) ** 2))
+            dk_den += float(np.sum(r["dk"] ** 2))
+            dv_num += float(np.sum((gpu["dvt"][b, kv][:, keys].T - r["dv"]) ** 2))
+            dv_den += float(np.sum(r["dv"] ** 2))
+    assert worst["o"] <= O_TOL, worst
+    assert worst["l"] <= L_TOL, worst
+    assert np.sqrt(dq_num / dq_den) <= GRAD_TOL
+    assert np.sqrt(dk_num / dk_den) <= GRAD_TOL
+    assert np.sqrt(dv_num / dv_den) <= GRAD_TOL
+    for name in ("o", "delta", "dq", "dk", "dvt"):
+        assert np.all(np.isfinite(gpu[name])), name
+    return worst
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("cfg", [3, 4, 5])
+def test_workload_sampled(cuda_device, cfg):
+    w = workloads.WORKLOADS[cfg]
+    inp = workloads.make_inputs(w)
+    gpu = run_gpu(inp, causal=w.causal, scale=w.scale)
+    rng = np.random.default_rng(100 + cfg)
+    B, H = w.batch, w.heads
+    G = w.group
+    if cfg == 4:
+        lens = inp["lens"]
+        batches = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 0, B - 1})
+        heads, kv_heads = [0, H - 1], [0]
+        # keys at or past a sequence's length have dK = dV = 0 exactly
+        for b in range(B):
+            n = int(lens[b])
+            assert np.all(gpu["dk"][b, :, n:] == 0.0)
+            assert np.all(gpu["dvt"][b, :, :, n:] == 0.0)
+            assert np.all(gpu["dq"][b, :, n:] == 0.0)
+    else:
+        batches = [0]
+        heads = [0, G - 1, H - 1]
+        kv_heads = [w.kv_heads - 1]
+    _check_sampled(w, inp, gpu, heads, kv_heads, batches, rng)
