@@ -26,7 +26,28 @@ struct DevState {
 };
 DevState g_dev[kMaxDevices];
 
-int device_ctx(DevCtx* ctx) {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+int device_context(DevCtx* ctx) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   DevState& s = g_dev[dev];
@@ -59,7 +80,7 @@ int device_ctx(DevCtx* ctx) {
 }
 
 // Admission checks (the pages' admission predicate, adapted: 64-bit offsets).
-int validate(const attn_shape* s, Dims* d) {
+int validate_shape(const attn_shape* s, Dims* d) {
   if (!s) return ATTN_ERR_NULL;
   if (s->batch < 1 || s->batch > 65535) return ATTN_ERR_SHAPE;
   if (s->seq < 64 || s->seq % 64 != 0 || s->seq > (1 << 22)) return ATTN_ERR_SHAPE;
@@ -93,30 +114,9 @@ int validate(const attn_shape* s, Dims* d) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-size_t workspace_bytes(const Dims& d) {
+size_t workspace_bytes_for(const Dims& d) {
   return (size_t)d.B * (size_t)(d.kv_count * d.G) * (size_t)d.npairs * kDsTileBytes;
 }
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static std::once_flag once;
-  static EncodeTiledFn fn = nullptr;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-}  // namespace
 
 bool encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                     uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1) {
@@ -150,6 +150,7 @@ const char* attn_error_string(int code) {
     case ATTN_ERR_CUDA: return "a CUDA call failed";
     case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";
     case ATTN_ERR_DEVICE: return "the current device is not sm_103";
+    case ATTN_ERR_SCRATCH_LIMIT: return "problem exceeds the static scratch of attn_bwd_noalloc";
     default: return "unknown error";
   }
 }
@@ -160,32 +161,32 @@ void attn_set_wait_limit_ns(uint64_t limit_ns) {
 
 size_t attn_bwd_workspace_bytes(const attn_shape* shape) {
   Dims d;
-  if (validate(shape, &d) != ATTN_OK) return 0;
-  return workspace_bytes(d);
+  if (validate_shape(shape, &d) != ATTN_OK) return 0;
+  return workspace_bytes_for(d);
 }
 
 int attn_fwd(const attn_shape* shape, const uint16_t* q, const uint16_t* k, const uint16_t* vt,
              uint16_t* o, float* lse, void* stream) {
   Dims d;
-  int rc = validate(shape, &d);
+  int rc = validate_shape(shape, &d);
   if (rc != ATTN_OK) return rc;
   if (!q || !k || !vt || !o || !lse) return ATTN_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_ALIGN;
   DevCtx ctx;
-  if ((rc = device_ctx(&ctx)) != ATTN_OK) return rc;
+  if ((rc = device_context(&ctx)) != ATTN_OK) return rc;
   return launch_fwd(d, ctx, q, k, vt, o, lse, static_cast<cudaStream_t>(stream));
 }
 
 int attn_row_terms(const attn_shape* shape, const uint16_t* o, const uint16_t* dout,
                    float* delta, void* stream) {
   Dims d;
-  int rc = validate(shape, &d);
+  int rc = validate_shape(shape, &d);
   if (rc != ATTN_OK) return rc;
   if (!o || !dout || !delta) return ATTN_ERR_NULL;
   if (!aligned16(o) || !aligned16(dout) || !aligned16(delta)) return ATTN_ERR_ALIGN;
   DevCtx ctx;
-  if ((rc = device_ctx(&ctx)) != ATTN_OK) return rc;
+  if ((rc = device_context(&ctx)) != ATTN_OK) return rc;
   return launch_row_terms(d, ctx, o, dout, delta, static_cast<cudaStream_t>(stream));
 }
 
@@ -194,15 +195,15 @@ int attn_bwd_keys(const attn_shape* shape, const uint16_t* q, const uint16_t* k,
                   const float* delta, void* ds_ws, size_t ws_bytes, float* dk, float* dvt,
                   void* stream) {
   Dims d;
-  int rc = validate(shape, &d);
+  int rc = validate_shape(shape, &d);
   if (rc != ATTN_OK) return rc;
   if (!q || !k || !vt || !dout || !lse || !delta || !ds_ws || !dk || !dvt) return ATTN_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(dout) || !aligned16(lse) ||
       !aligned16(delta) || !aligned16(ds_ws) || !aligned16(dk) || !aligned16(dvt))
     return ATTN_ERR_ALIGN;
-  if (ws_bytes < workspace_bytes(d)) return ATTN_ERR_WORKSPACE;
+  if (ws_bytes < workspace_bytes_for(d)) return ATTN_ERR_WORKSPACE;
   DevCtx ctx;
-  if ((rc = device_ctx(&ctx)) != ATTN_OK) return rc;
+  if ((rc = device_context(&ctx)) != ATTN_OK) return rc;
   return launch_bwd_keys(d, ctx, q, k, vt, dout, lse, delta, static_cast<uint8_t*>(ds_ws), dk,
                          dvt, static_cast<cudaStream_t>(stream));
 }
@@ -210,20 +211,20 @@ int attn_bwd_keys(const attn_shape* shape, const uint16_t* q, const uint16_t* k,
 int attn_bwd_queries(const attn_shape* shape, const uint16_t* k, const void* ds_ws,
                      size_t ws_bytes, float* dq, void* stream) {
   Dims d;
-  int rc = validate(shape, &d);
+  int rc = validate_shape(shape, &d);
   if (rc != ATTN_OK) return rc;
   if (!k || !ds_ws || !dq) return ATTN_ERR_NULL;
   if (!aligned16(k) || !aligned16(ds_ws) || !aligned16(dq)) return ATTN_ERR_ALIGN;
-  if (ws_bytes < workspace_bytes(d)) return ATTN_ERR_WORKSPACE;
+  if (ws_bytes < workspace_bytes_for(d)) return ATTN_ERR_WORKSPACE;
   DevCtx ctx;
-  if ((rc = device_ctx(&ctx)) != ATTN_OK) return rc;
+  if ((rc = device_context(&ctx)) != ATTN_OK) return rc;
   return launch_bwd_queries(d, ctx, k, static_cast<const uint8_t*>(ds_ws), dq,
                             static_cast<cudaStream_t>(stream));
 }
 
 int attn_last_device_error(void* stream) {
   DevCtx ctx;
-  int rc = device_ctx(&ctx);
+  int rc = device_context(&ctx);
   if (rc != ATTN_OK) return rc;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
@@ -237,7 +238,7 @@ int attn_last_device_error(void* stream) {
 
 int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   DevCtx ctx;
-  int rc = device_ctx(&ctx);
+  int rc = device_context(&ctx);
   if (rc != ATTN_OK) return rc;
   rc = launch_wait_probe(ctx, limit_ns ? limit_ns : 1000000ull, static_cast<cudaStream_t>(stream));
   if (rc != ATTN_OK) return rc;

@@ -38,6 +38,16 @@ struct DevCtx {
   int sm_count;
 };
 
+// Host-side admission checks of a shape (ATTN_OK or an ATTN_ERR_ code) and
+// the derived sizes.
+int validate_shape(const attn_shape* s, Dims* d);
+// The current device's context (error word, SM count, wait limit); fails
+// with ATTN_ERR_DEVICE on anything but sm_103.
+int device_context(DevCtx* ctx);
+// Bytes of the dS workspace for a validated shape and its head chunk.
+size_t workspace_bytes_for(const Dims& d);
+bool aligned16(const void* p);
+
 // Encodes a rank-3 binary16 tiled tensor map with the 128-byte swizzle.
 // dims/strides as cuTensorMapEncodeTiled takes them (strides in bytes of
 // dims 1 and 2), box = {box0, box1, 1}.

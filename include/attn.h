@@ -66,8 +66,13 @@ enum {
   ATTN_ERR_WORKSPACE = -4,      /* workspace smaller than required           */
   ATTN_ERR_CUDA = -5,           /* a CUDA runtime/driver call failed         */
   ATTN_ERR_DEVICE_TIMEOUT = -6, /* a kernel's bounded wait ran out           */
-  ATTN_ERR_DEVICE = -7          /* the current device is not sm_103          */
+  ATTN_ERR_DEVICE = -7,         /* the current device is not sm_103          */
+  ATTN_ERR_SCRATCH_LIMIT = -8   /* attn_bwd_noalloc: problem exceeds its
+                                   static scratch                            */
 };
+
+/* Size of the static device scratch that attn_bwd_noalloc works in. */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)128 << 20)
 
 /*
  * Problem shape.  Admission (the pages' admission predicate, "the program"
@@ -149,6 +154,43 @@ ATTN_API int attn_bwd_keys(const attn_shape* shape, const uint16_t* q, const uin
 ATTN_API int attn_bwd_queries(const attn_shape* shape, const uint16_t* k,
                      const void* ds_ws, size_t ws_bytes, float* dq,
                      void* stream);
+
+/*
+ * attn_bwd_noalloc - the key pass and the dQ pass (what attn_bwd_keys and
+ * then attn_bwd_queries compute) without a caller-supplied workspace.  The
+ * method's pages have no counterpart to this entry point.  It is for callers
+ * that may not allocate device memory while they run: for example a plugin
+ * or custom-operator interface whose execute step must not allocate because
+ * the host framework owns all device memory, or a latency-bound loop that
+ * cannot take the implicit device synchronisation of cudaMalloc.
+ *
+ * The dS scratch lives in a static device array of
+ * ATTN_NOALLOC_SCRATCH_BYTES (128 MiB) inside the library; every GPU on
+ * which the library's code is loaded holds that array until the process
+ * exits.  The call walks the chunk's K/V heads in groups that fit the array,
+ * and calls no cudaMalloc, cudaFree or other allocating routine.  The first
+ * call on a device looks up the array's device address (once per device,
+ * with that device current); make that first call before any stream capture.
+ *
+ * Arguments as attn_bwd_keys and attn_bwd_queries (device pointers, 16-byte
+ * aligned, layouts in the file header): reads q, k, vt, dout, lse, delta;
+ * writes dq, dk, dvt for the K/V heads of the shape's head chunk (0, 0 = all)
+ * and their query heads.  Returns ATTN_ERR_SCRATCH_LIMIT, before launching
+ * anything, when one K/V head's share (batch x query heads per K/V head x
+ * dS tiles of one head x 32 KiB) exceeds the array; other errors as the
+ * other entry points.
+ *
+ * Every call, on every stream and host thread, shares the one array, and a
+ * call leaves its dS tiles there.  Nothing in the array has to start at
+ * zero: each tile the dQ pass reads was written earlier in the same call.
+ * Calls whose work overlaps on the GPU race on the array and give wrong
+ * results: order them on one stream or synchronise between them.
+ */
+ATTN_API int attn_bwd_noalloc(const attn_shape* shape, const uint16_t* q,
+                              const uint16_t* k, const uint16_t* vt,
+                              const uint16_t* dout, const float* lse,
+                              const float* delta, float* dq, float* dk,
+                              float* dvt, void* stream);
 
 /* A static, human-readable message for an ATTN_ code. */
 ATTN_API const char* attn_error_string(int code);

@@ -102,7 +102,7 @@ def test_workspace_bytes_closed_form(lib, B, T, H, Hkv, causal, count):
 
 
 def test_error_strings(lib):
-    for code in range(-7, 1):
+    for code in range(-8, 1):
         msg = api.error_string(code)
         assert msg and msg != "unknown error"
     assert api.error_string(-99) == "unknown error"
