@@ -1,6 +1,6 @@
 // bwd_keys.cu - the key pass of the backward: one 128-key tile of one K/V
 // head per CTA, walking every query head of the head's group and every
-// 128-query tile that can see the keys.
+// 64-query half of each 128-query tile that can see the keys.
 //
 // Method (StreamingAttentionSM86.alpha, key launch streamingAttentionKeySM86
 // and the page-1 header of the split backward): with L and D of the queries,
@@ -11,15 +11,26 @@
 // pass's sksStoreScoreGradients), so S, P and dP are formed once.  The
 // epilogue writes dK = s * sum (binary32 rows) and dV^T unscaled.
 //
-// GB300 design: warps 0-3 one thread per key row (tensor-memory lane),
-// warp 4 TMA producer (K and V^T once, Q / dO / L / D per step through a
-// 2-stage ring), warp 5 MMA issuer.  The group's query heads are summed in
-// the tensor-memory accumulators of dK and dV (no atomics, fixed order).
-// dS^T goes through shared memory in the 128-byte-swizzled image that both
-// the dK product here (K-major A) and the dQ pass (MN-major A) read, and is
-// copied to the workspace by one bulk store per step.
-// Tensor memory: S^T 0-127, dP^T 128-255, P^T 256-319 (binary16 pairs),
-// dK 320-383, dV 384-447.
+// GB300 design.
+//   warps 0-7  score gradients, thread = key row (tensor-memory lane); warps
+//              0-3 take queries 0-31 of a step, warps 4-7 queries 32-63
+//   warp 8     TMA producer: K and V^T once, then per step a 64-query tile of
+//              Q and dO and their L and D, through a 4-stage ring
+//   warp 9     MMA issuer
+// K and V are copied once into tensor memory and are the A operands of
+// S^T = K Q^T and dP^T = V dO^T; P^T and dS^T are written to tensor memory
+// and are the A operands of dV += P^T dO and dK += dS^T Q (Q and dO read
+// MN-major from their tiles), so the tensor core reads only the 8 KiB Q / dO
+// tiles from shared memory.  S^T and dP^T are double-buffered: the MMAs of
+// step n+1 run while the score-gradient warps work on step n.  The group's
+// query heads are summed in the tensor-memory accumulators of dK and dV (no
+// atomics, fixed order).  dS^T also goes to shared memory in the
+// 128-byte-swizzled image that the dQ pass reads, and one 16 KiB bulk store
+// per step copies it into the workspace.
+//
+// Tensor memory (512 columns): K 0-31, V 32-63 (binary16 pairs); S^T / dP^T
+// buffer b at 64+128b / 128+128b (64 columns each); P^T 320-351 and dS^T
+// 352-383 (binary16 pairs); dK 384-447, dV 448-511.
 #include <math.h>
 
 #include <mutex>
@@ -31,34 +42,36 @@ namespace css {
 namespace {
 
 constexpr int kBK = 128;  // keys per CTA
-constexpr int kBQ = 128;  // queries per step
-constexpr int kThreads = 192;
-constexpr int kStages = 2;
-constexpr uint32_t kTileB = 16384;  // 128 rows x 128 B
-constexpr uint32_t kSmemK = 0;
-constexpr uint32_t kSmemV = kTileB;  // V^T: two 64-key halves of 64 rows x 128 B
-constexpr uint32_t kSmemStage0 = 2 * kTileB;
-constexpr uint32_t kStageQ = 0, kStageDO = kTileB, kStageL = 2 * kTileB, kStageD = 2 * kTileB + 512;
-constexpr uint32_t kStageBytes = 2 * kTileB + 2048;  // keeps every stage 1024-aligned
+constexpr int kBQ = 64;   // queries per step
+constexpr int kThreads = 320;
+constexpr int kStages = 4;
+constexpr uint32_t kSmemK = 0;                // K tile: 128 rows x 128 B
+constexpr uint32_t kSmemV = 16384;            // V^T: two 64-key halves of 64 rows x 128 B
+constexpr uint32_t kSmemStage0 = 32768;
+constexpr uint32_t kStQ = 0, kStDO = 8192, kStL = 16384, kStD = 16640;
+constexpr uint32_t kStageBytes = 17408;       // a multiple of 1024
 constexpr uint32_t kSmemDS0 = kSmemStage0 + kStages * kStageBytes;
-constexpr uint32_t kSmemBar = kSmemDS0 + 2 * kDsTileBytes;
+constexpr uint32_t kDSHalf = 16384;           // one 64-query half of a workspace tile
+constexpr uint32_t kSmemBar = kSmemDS0 + 2 * kDSHalf;
 constexpr uint32_t kSmemBytes = kSmemBar + 256 + 1024;
 
-constexpr uint32_t kColST = 0, kColDPT = 128, kColPT = 256, kColDK = 320, kColDV = 384;
+constexpr uint32_t kColK = 0, kColV = 32, kColS0 = 64, kColPT = 320, kColDST = 352,
+                   kColDK = 384, kColDV = 448;
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);   // K (K-major) x Q (K-major)
-constexpr uint32_t kIdescDP = idesc_f16_f32(128, 128, 1, 0);  // V (MN-major) x dO (K-major)
-constexpr uint32_t kIdescAcc = idesc_f16_f32(128, 64, 0, 1);  // P^T/dS^T x dO/Q (MN-major)
+constexpr uint32_t kIdescS = idesc_f16_f32(128, 64, 0, 0);    // A (tmem) x Q / dO (K-major)
+constexpr uint32_t kIdescAcc = idesc_f16_f32(128, 64, 0, 1);  // A (tmem) x dO / Q (MN-major)
 
 enum {
-  BAR_KV = 0,
-  BAR_Q_FULL = 1,
+  BAR_KV_FULL = 0,
+  BAR_KV_TMEM,
+  BAR_Q_FULL,
   BAR_Q_EMPTY = BAR_Q_FULL + kStages,
-  BAR_S_FULL = BAR_Q_EMPTY + kStages,
-  BAR_P_READY,
-  BAR_DS_FREE,                     // [2] the dK product has read dS^T buffer b
-  BAR_DS_STORED = BAR_DS_FREE + 2,  // [2] the bulk store has read dS^T buffer b
+  BAR_S_FULL = BAR_Q_EMPTY + kStages,  // [2]
+  BAR_ST_FREE = BAR_S_FULL + 2,        // [2]
+  BAR_P_READY = BAR_ST_FREE + 2,
+  BAR_PT_FREE,
+  BAR_DS_STORED,  // [2]
   BAR_DONE = BAR_DS_STORED + 2,
   BAR_COUNT
 };
@@ -82,6 +95,38 @@ static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, ui
   while (!mbar_try_wait(bar, parity))
     if (global_timer_ns() - t0 > limit_ns) return false;
   return true;
+}
+
+// Score gradients of 32 queries for one key row: P = 2^(S c - L),
+// dS = P (dP - D), both packed to binary16 pairs.  MASK zeroes the entries
+// outside [qlo, qhi) (local query indices).
+template <bool MASK>
+__device__ __forceinline__ void score_gradients(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
+                                                const float4* __restrict__ L4,
+                                                const float4* __restrict__ D4, float c, int qlo,
+                                                int qhi, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
+  const float2 c2 = make_float2(c, c);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const float4 l = L4[u];
+    const float4 dl = D4[u];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = 4 * u + 2 * h;
+      const float2 nl = h ? make_float2(-l.z, -l.w) : make_float2(-l.x, -l.y);
+      const float2 nd = h ? make_float2(-dl.z, -dl.w) : make_float2(-dl.x, -dl.y);
+      const float2 t = __ffma2_rn(make_float2(as_f(sv[e]), as_f(sv[e + 1])), c2, nl);
+      float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+      const float2 g = __fadd2_rn(make_float2(as_f(dv[e]), as_f(dv[e + 1])), nd);
+      float2 ds = __fmul2_rn(p, g);
+      if (MASK) {
+        if (e < qlo || e >= qhi) p.x = 0.f, ds.x = 0.f;
+        if (e + 1 < qlo || e + 1 >= qhi) p.y = 0.f, ds.y = 0.f;
+      }
+      pp[e >> 1] = pack_f16x2(p.x, p.y);
+      dd[e >> 1] = pack_f16x2(ds.x, ds.y);
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -112,36 +157,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int k0 = jt * kBK;
   const int i_lo = d.causal ? jt : 0;
-  int i_hi = (len + kBQ - 1) / kBQ;
+  int i_hi = (len + kTile - 1) / kTile;
   if (k0 >= len) i_hi = i_lo;
   const int n_i = i_hi > i_lo ? i_hi - i_lo : 0;
-  const int n_steps = d.G * n_i;
+  // 64-query halves per query head: the second half of a tile that starts at
+  // or past T holds no row and is skipped (its rows are never stored).
+  const bool half_tail = n_i > 0 && (i_hi - 1) * kTile + kBQ >= T;
+  const int per_g = n_i > 0 ? 2 * n_i - (half_tail ? 1 : 0) : 0;
+  const int n_steps = d.G * per_g;
 
   WaitCtl wc{a.err, a.wait_ns, &s_abort};
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    mbar_init(BAR(BAR_KV), 1);
+    mbar_init(BAR(BAR_KV_FULL), 1);
+    mbar_init(BAR(BAR_KV_TMEM), 256);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(BAR(BAR_Q_FULL + s), 1);
       mbar_init(BAR(BAR_Q_EMPTY + s), 1);
     }
-    mbar_init(BAR(BAR_S_FULL), 1);
-    mbar_init(BAR(BAR_P_READY), 128);
     for (int u = 0; u < 2; ++u) {
-      mbar_init(BAR(BAR_DS_FREE + u), 1);
+      mbar_init(BAR(BAR_S_FULL + u), 1);
+      mbar_init(BAR(BAR_ST_FREE + u), 256);
       mbar_init(BAR(BAR_DS_STORED + u), 1);
     }
+    mbar_init(BAR(BAR_P_READY), 256);
+    mbar_init(BAR(BAR_PT_FREE), 1);
     mbar_init(BAR(BAR_DONE), 1);
     fence_mbarrier_init();
   }
-  if (warp == 5) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+  if (warp == 9) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- TMA producer ----------------
     if (lane == 0 && n_steps > 0) {
       tma_prefetch_desc(&tm_q);
@@ -149,201 +200,231 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_vt);
       tma_prefetch_desc(&tm_do);
       const int kvplane = b * d.Hkv + kv;
-      mbar_arrive_expect_tx(BAR(BAR_KV), 2 * kTileB);
-      tma_load_3d(sbase + kSmemK, &tm_k, BAR(BAR_KV), 0, k0, kvplane);
-      tma_load_3d(sbase + kSmemV, &tm_vt, BAR(BAR_KV), k0, 0, kvplane);
-      tma_load_3d(sbase + kSmemV + 8192, &tm_vt, BAR(BAR_KV), k0 + 64, 0, kvplane);
+      mbar_arrive_expect_tx(BAR(BAR_KV_FULL), 32768);
+      tma_load_3d(sbase + kSmemK, &tm_k, BAR(BAR_KV_FULL), 0, k0, kvplane);
+      tma_load_3d(sbase + kSmemV, &tm_vt, BAR(BAR_KV_FULL), k0, 0, kvplane);
+      tma_load_3d(sbase + kSmemV + 8192, &tm_vt, BAR(BAR_KV_FULL), k0 + 64, 0, kvplane);
       int issued = 0;
       for (int n = 0; n < n_steps; ++n) {
         const int s = n % kStages;
         if (n >= kStages && !mbar_wait(BAR(BAR_Q_EMPTY + s), ((n / kStages) - 1) & 1, wc)) break;
-        const int g = n / n_i;
-        const int i = i_lo + n % n_i;
+        const int g = n / per_g;
+        const int rem = n - g * per_g;
+        const int q0 = (i_lo + (rem >> 1)) * kTile + (rem & 1) * kBQ;
         const int qplane = b * d.H + kv * d.G + g;
-        const int rows = min(kBQ, T - i * kBQ);
         const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
-        mbar_arrive_expect_tx(BAR(BAR_Q_FULL + s), 2 * kTileB + 2 * rows * 4);
-        tma_load_3d(st + kStageQ, &tm_q, BAR(BAR_Q_FULL + s), 0, i * kBQ, qplane);
-        tma_load_3d(st + kStageDO, &tm_do, BAR(BAR_Q_FULL + s), 0, i * kBQ, qplane);
-        const size_t lo = (size_t)qplane * T + (size_t)i * kBQ;
-        bulk_load(st + kStageL, a.lse + lo, rows * 4, BAR(BAR_Q_FULL + s));
-        bulk_load(st + kStageD, a.delta + lo, rows * 4, BAR(BAR_Q_FULL + s));
+        mbar_arrive_expect_tx(BAR(BAR_Q_FULL + s), 2 * 8192 + 2 * kBQ * 4);
+        tma_load_3d(st + kStQ, &tm_q, BAR(BAR_Q_FULL + s), 0, q0, qplane);
+        tma_load_3d(st + kStDO, &tm_do, BAR(BAR_Q_FULL + s), 0, q0, qplane);
+        const size_t lo = (size_t)qplane * T + (size_t)q0;
+        bulk_load(st + kStL, a.lse + lo, kBQ * 4, BAR(BAR_Q_FULL + s));
+        bulk_load(st + kStD, a.delta + lo, kBQ * 4, BAR(BAR_Q_FULL + s));
         issued = n + 1;
       }
-      drain_wait(BAR(BAR_KV), 0, a.wait_ns);
+      drain_wait(BAR(BAR_KV_FULL), 0, a.wait_ns);
       for (int n = (issued > kStages ? issued - kStages : 0); n < issued; ++n)
         drain_wait(BAR(BAR_Q_FULL + n % kStages), (n / kStages) & 1, a.wait_ns);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------- MMA issuer (one thread) ----------------
     if (lane == 0 && n_steps > 0) {
-      const uint32_t k_s = sbase + kSmemK, v_s = sbase + kSmemV;
-      bool ok = mbar_wait(BAR(BAR_KV), 0, wc);
-      for (int n = 0; ok && n < n_steps; ++n) {
+      bool ok = mbar_wait(BAR(BAR_KV_TMEM), 0, wc);
+      tc_fence_after();
+      // dV += P^T dO and dK += dS^T Q of step m (stage m % kStages); the
+      // reduction runs over the step's 64 queries, 16 rows (2 KiB) per K step
+      auto accumulate = [&](int m) -> bool {
+        if (!mbar_wait(BAR(BAR_P_READY), m & 1, wc)) return false;
+        tc_fence_after();
+        const uint32_t st = sbase + kSmemStage0 + (m % kStages) * kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(tmem + kColDV, tmem + kColPT + kk * 8,
+                 sdesc_sw128(st + kStDO + kk * 2048, 8192, 1024), kIdescAcc,
+                 (m > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(tmem + kColDK, tmem + kColDST + kk * 8,
+                 sdesc_sw128(st + kStQ + kk * 2048, 8192, 1024), kIdescAcc,
+                 (m > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(BAR(BAR_Q_EMPTY + m % kStages));
+        mma_commit(BAR(BAR_PT_FREE));
+        return true;
+      };
+      int n = 0;
+      for (; ok && n < n_steps; ++n) {
         const int s = n % kStages;
+        const int buf = n & 1;
         if (!mbar_wait(BAR(BAR_Q_FULL + s), (n / kStages) & 1, wc)) break;
+        if (n >= 2 && !mbar_wait(BAR(BAR_ST_FREE + buf), ((n >> 1) - 1) & 1, wc)) break;
         tc_fence_after();
         const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
-        const uint32_t q_s = st + kStageQ, do_s = st + kStageDO;
-        // S^T = K Q^T (reduction over d: four K=16 steps of 32 B)
+        const uint32_t c_s = kColS0 + 128 * buf;
+        // S^T = K Q^T and dP^T = V dO^T (reduction over d: four K=16 steps)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tmem + kColST, sdesc_sw128(k_s + kk * 32, 16, 1024),
-                 sdesc_sw128(q_s + kk * 32, 16, 1024), kIdescS, kk > 0);
-        // dP^T = V dO^T: V read MN-major from the V^T tile (keys along the
-        // 128-byte rows, two 64-key blocks 8 KiB apart; a K step = 16 rows)
+          mma_ts(tmem + c_s, tmem + kColK + kk * 8, sdesc_sw128(st + kStQ + kk * 32, 16, 1024),
+                 kIdescS, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tmem + kColDPT, sdesc_sw128(v_s + kk * 2048, 8192, 1024),
-                 sdesc_sw128(do_s + kk * 32, 16, 1024), kIdescDP, kk > 0);
-        mma_commit(BAR(BAR_S_FULL));
-        if (!mbar_wait(BAR(BAR_P_READY), n & 1, wc)) break;
-        tc_fence_after();
-        const uint32_t ds_s = sbase + kSmemDS0 + (n & 1) * kDsTileBytes;
-        // dV += P^T dO and dK += dS^T Q: reduction over the step's 128
-        // queries (eight K=16 steps); dO and Q read MN-major (d along rows).
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + kColDV, tmem + kColPT + kk * 8, sdesc_sw128(do_s + kk * 2048, 8192, 1024),
-                 kIdescAcc, (n > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + kColDK, sdesc_sw128(ds_s + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(q_s + kk * 2048, 8192, 1024), kIdescAcc, (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(BAR(BAR_Q_EMPTY + s));
-        mma_commit(BAR(BAR_DS_FREE + (n & 1)));
+          mma_ts(tmem + c_s + 64, tmem + kColV + kk * 8,
+                 sdesc_sw128(st + kStDO + kk * 32, 16, 1024), kIdescS, kk > 0);
+        mma_commit(BAR(BAR_S_FULL + buf));
+        if (n >= 1 && !accumulate(n - 1)) {
+          ok = false;
+          break;
+        }
       }
+      if (ok && n == n_steps) accumulate(n_steps - 1);
       mma_commit(BAR(BAR_DONE));
     }
   } else {
     // ---------------- score gradients: thread = key row ----------------
-    const int kr = threadIdx.x;
-    const int key = k0 + kr;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int wg = warp >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int key = k0 + r;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float c = d.c;
-    const int h_local0 = (kv - d.kv_begin) * d.G;
     const int Hc = d.kv_count * d.G;
+    const int h_local0 = (kv - d.kv_begin) * d.G;
     bool ok = true;
-    for (int n = 0; n < n_steps; ++n) {
-      const int s = n % kStages;
-      const int g = n / n_i;
-      const int i = i_lo + n % n_i;
-      const uint32_t ds_s = sbase + kSmemDS0 + (n & 1) * kDsTileBytes;
-      if (n >= 2) {
-        // dS^T buffer n%2 was last filled at step n-2: wait until the dK
-        // product and the bulk store of that step have both read it
-        if (!mbar_wait(BAR(BAR_DS_FREE + (n & 1)), ((n >> 1) - 1) & 1, wc) ||
-            !mbar_wait(BAR(BAR_DS_STORED + (n & 1)), ((n >> 1) - 1) & 1, wc)) {
-          ok = false;
-          break;
+    if (n_steps > 0) {
+      // K (warps 0-3) or V (warps 4-7) row r into tensor memory as A operands
+      ok = mbar_wait_warp(BAR(BAR_KV_FULL), 0, wc);
+      uint32_t w[32];
+      if (wg == 0) {
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 v = *reinterpret_cast<const uint4*>(sgen + kSmemK + sw128_offset(r, ch));
+          w[4 * ch] = v.x, w[4 * ch + 1] = v.y, w[4 * ch + 2] = v.z, w[4 * ch + 3] = v.w;
+        }
+      } else {
+        // V^T tile: row = d, 64 keys per 128-byte row, keys 64-127 in the second half
+        const uint8_t* vt = sgen + kSmemV + (r >> 6) * 8192;
+        const int kc = (r & 63) >> 3, kb = (r & 7) * 2;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const uint32_t lo =
+              *reinterpret_cast<const uint16_t*>(vt + sw128_offset(2 * u, kc) + kb);
+          const uint32_t hi =
+              *reinterpret_cast<const uint16_t*>(vt + sw128_offset(2 * u + 1, kc) + kb);
+          w[u] = lo | (hi << 16);
         }
       }
-      if (!mbar_wait(BAR(BAR_S_FULL), n & 1, wc)) {
+      tmem_st32(tmem + lane_base + (wg == 0 ? kColK : kColV), w);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(BAR(BAR_KV_TMEM));
+    }
+    for (int n = 0; ok && n < n_steps; ++n) {
+      const int s = n % kStages;
+      const int buf = n & 1;
+      const int g = n / per_g;
+      const int rem = n - g * per_g;
+      const int it = i_lo + (rem >> 1);
+      const int hq = rem & 1;
+      const int qb = it * kTile + hq * kBQ + 32 * wg;  // this thread's first query
+      if (!mbar_wait_warp(BAR(BAR_S_FULL + buf), (n >> 1) & 1, wc)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      uint32_t sv[32], dv[32];
+      const uint32_t c_s = kColS0 + 128 * buf + 32 * wg;
+      tmem_ld32x2_wait(tmem + lane_base + c_s, tmem + lane_base + c_s + 64, sv, dv);
+      tc_fence_before();
+      mbar_arrive(BAR(BAR_ST_FREE + buf));
+
       const uint8_t* stg = sgen + kSmemStage0 + s * kStageBytes;
-      const float* Ls = reinterpret_cast<const float*>(stg + kStageL);
-      const float* Ds = reinterpret_cast<const float*>(stg + kStageD);
-      const int q0 = i * kBQ;
-      const bool need_mask = (d.causal && q0 < k0 + kBK) || (q0 + kBQ > len) || (k0 + kBK > len);
-      // query (local index) ql is valid for this key iff qlo <= ql < qhi
-      const int qlo = (d.causal ? key : 0) - q0;
-      const int qhi = (key < len ? len : 0) - q0;
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32x2_wait(tmem + lane_base + kColST + ch * 32, tmem + lane_base + kColDPT + ch * 32,
-                         sv, dv);
-        uint32_t pp[16], dd[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int ql = ch * 32 + e;
-          float p0 = ex2_approx(fmaf(as_f(sv[e]), c, -Ls[ql]));
-          float p1 = ex2_approx(fmaf(as_f(sv[e + 1]), c, -Ls[ql + 1]));
-          float d0 = p0 * (as_f(dv[e]) - Ds[ql]);
-          float d1 = p1 * (as_f(dv[e + 1]) - Ds[ql + 1]);
-          if (need_mask) {
-            if (ql < qlo || ql >= qhi) p0 = 0.f, d0 = 0.f;
-            if (ql + 1 < qlo || ql + 1 >= qhi) p1 = 0.f, d1 = 0.f;
-          }
-          pp[e >> 1] = pack_f16x2(p0, p1);
-          dd[e >> 1] = pack_f16x2(d0, d1);
-        }
-        tmem_st16(tmem + lane_base + kColPT + ch * 16, pp);
-        // dS^T row kr, queries 32ch..32ch+31: 64-query block ch/2, chunks
-        // (ch%2)*4 .. +3 of the swizzled 128-byte row
-        const uint32_t rowbase = ds_s + (ch >> 1) * 16384;
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          st_shared_v4(rowbase + sw128_offset(kr, (ch & 1) * 4 + u), dd[4 * u], dd[4 * u + 1],
-                       dd[4 * u + 2], dd[4 * u + 3]);
+      const float4* L4 = reinterpret_cast<const float4*>(stg + kStL) + 8 * wg;
+      const float4* D4 = reinterpret_cast<const float4*>(stg + kStD) + 8 * wg;
+      const bool need_mask =
+          (d.causal && qb < k0 + kBK - 1) || (qb + 32 > len) || (k0 + kBK > len);
+      const int qlo = (d.causal ? key : 0) - qb;
+      const int qhi = (key < len ? len : 0) - qb;
+      uint32_t pp[16], dd[16];
+      if (need_mask)
+        score_gradients<true>(sv, dv, L4, D4, c, qlo, qhi, pp, dd);
+      else
+        score_gradients<false>(sv, dv, L4, D4, c, qlo, qhi, pp, dd);
+
+      // P^T / dS^T columns: dV and dK of the previous step have read them
+      if (n >= 1 && !mbar_wait_warp(BAR(BAR_PT_FREE), (n - 1) & 1, wc)) {
+        ok = false;
+        break;
       }
+      // shared dS^T buffer: the bulk store of step n-2 has read it
+      if (n >= 2 && !mbar_wait_warp(BAR(BAR_DS_STORED + buf), ((n >> 1) - 1) & 1, wc)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st16(tmem + lane_base + kColPT + 16 * wg, pp);
+      tmem_st16(tmem + lane_base + kColDST + 16 * wg, dd);
+      // dS^T row r, queries 32wg..32wg+31 of this 64-query half: chunks 4wg..4wg+3
+      const uint32_t dsb = sbase + kSmemDS0 + buf * kDSHalf;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        st_shared_v4(dsb + sw128_offset(r, 4 * wg + u), dd[4 * u], dd[4 * u + 1], dd[4 * u + 2],
+                     dd[4 * u + 3]);
       tmem_st_wait();
       tc_fence_before();
       fence_proxy_async_shared();
       mbar_arrive(BAR(BAR_P_READY));
-      if (threadIdx.x == 0) {
-        // every row of dS^T is in shared memory once all 128 threads arrived
-        if (!mbar_wait(BAR(BAR_P_READY), n & 1, wc)) {
-          ok = false;
-          break;
-        }
-        const long long tile =
-            ((long long)b * Hc + h_local0 + g) * d.npairs + d.pair(i, jt);
-        bulk_store(a.ws + (size_t)tile * kDsTileBytes, ds_s, kDsTileBytes);
+      bool stored = true;
+      if (threadIdx.x == 0 && (stored = mbar_wait(BAR(BAR_P_READY), n & 1, wc))) {
+        const long long tile = ((long long)b * Hc + h_local0 + g) * d.npairs + d.pair(it, jt);
+        bulk_store(a.ws + (size_t)tile * kDsTileBytes + (size_t)hq * kDSHalf, dsb, kDSHalf);
         bulk_commit();
         if (n >= 1) {
-          // at most this step's store still reads shared memory: the
-          // previous step's buffer is free for step n+1
+          // at most this step's store still reads shared memory
           bulk_wait_read<1>();
           mbar_arrive(BAR(BAR_DS_STORED + ((n - 1) & 1)));
         }
+      }
+      if (warp == 0) stored = __shfl_sync(0xffffffffu, stored, 0);
+      if (!stored) {
+        ok = false;
+        break;
       }
     }
     if (threadIdx.x == 0) bulk_wait_all<0>();
 
     // ---------------- epilogue: dK = s * sum (rows), dV^T (columns) ----------------
     const bool store = key < T;
-    float* dkrow = a.dk + (((size_t)b * d.Hkv + kv) * T + key) * 64;
-    float* dvcol = a.dvt + ((size_t)b * d.Hkv + kv) * 64 * (size_t)T + key;
+    uint32_t r0[32], r1[32];
     if (n_steps > 0) {
       ok = ok && mbar_wait(BAR(BAR_DONE), 0, wc);
       tc_fence_after();
-      uint32_t r0[32], r1[32];
-      tmem_ld32x2_wait(tmem + lane_base + kColDK, tmem + lane_base + kColDK + 32, r0, r1);
-      if (store) {
-        float4* dst = reinterpret_cast<float4*>(dkrow);
+      const uint32_t col = wg == 0 ? kColDK : kColDV;
+      tmem_ld32x2_wait(tmem + lane_base + col, tmem + lane_base + col + 32, r0, r1);
+    } else {
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          dst[u] = make_float4(as_f(r0[4 * u]) * d.scale, as_f(r0[4 * u + 1]) * d.scale,
-                               as_f(r0[4 * u + 2]) * d.scale, as_f(r0[4 * u + 3]) * d.scale);
+      for (int u = 0; u < 32; ++u) r0[u] = r1[u] = 0u;
+    }
+    if (store && wg == 0) {
+      float4* dst = reinterpret_cast<float4*>(a.dk + (((size_t)b * d.Hkv + kv) * T + key) * 64);
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          dst[8 + u] = make_float4(as_f(r1[4 * u]) * d.scale, as_f(r1[4 * u + 1]) * d.scale,
-                                   as_f(r1[4 * u + 2]) * d.scale, as_f(r1[4 * u + 3]) * d.scale);
-      }
-      tmem_ld32x2_wait(tmem + lane_base + kColDV, tmem + lane_base + kColDV + 32, r0, r1);
-      if (store) {
+      for (int u = 0; u < 8; ++u)
+        dst[u] = make_float4(as_f(r0[4 * u]) * d.scale, as_f(r0[4 * u + 1]) * d.scale,
+                             as_f(r0[4 * u + 2]) * d.scale, as_f(r0[4 * u + 3]) * d.scale);
 #pragma unroll
-        for (int u = 0; u < 32; ++u) dvcol[(size_t)u * T] = as_f(r0[u]);
-#pragma unroll
-        for (int u = 0; u < 32; ++u) dvcol[(size_t)(32 + u) * T] = as_f(r1[u]);
-      }
+      for (int u = 0; u < 8; ++u)
+        dst[8 + u] = make_float4(as_f(r1[4 * u]) * d.scale, as_f(r1[4 * u + 1]) * d.scale,
+                                 as_f(r1[4 * u + 2]) * d.scale, as_f(r1[4 * u + 3]) * d.scale);
     } else if (store) {
-      float4* dst = reinterpret_cast<float4*>(dkrow);
+      float* dvcol = a.dvt + ((size_t)b * d.Hkv + kv) * 64 * (size_t)T + key;
 #pragma unroll
-      for (int u = 0; u < 16; ++u) dst[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < 32; ++u) dvcol[(size_t)u * T] = as_f(r0[u]);
 #pragma unroll
-      for (int u = 0; u < 64; ++u) dvcol[(size_t)u * T] = 0.f;
+      for (int u = 0; u < 32; ++u) dvcol[(size_t)(32 + u) * T] = as_f(r1[u]);
     }
     (void)ok;
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     if (n_steps > 0) drain_wait(BAR(BAR_DONE), 0, a.wait_ns);
     __syncwarp();

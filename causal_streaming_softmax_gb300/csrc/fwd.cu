@@ -76,6 +76,82 @@ static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, ui
   return true;
 }
 
+// The row's maximum raw score over one 128-key tile in tensor memory.  MASK
+// sets the columns at or past `lim` (local key index) to -inf first.
+template <bool MASK>
+__device__ __forceinline__ float tile_row_max(uint32_t t_s, int lim) {
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t v0[32], v1[32];
+    tmem_ld32x2_wait(t_s + half * 64, t_s + half * 64 + 32, v0, v1);
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      float x0 = as_f(v0[e]), x1 = as_f(v0[e + 1]), y0 = as_f(v1[e]), y1 = as_f(v1[e + 1]);
+      if (MASK) {
+        const int cb = half * 64 + e;
+        if (cb >= lim) x0 = -INFINITY;
+        if (cb + 1 >= lim) x1 = -INFINITY;
+        if (cb + 32 >= lim) y0 = -INFINITY;
+        if (cb + 33 >= lim) y1 = -INFINITY;
+      }
+      if (e & 2) {
+        m0 = fmax3(m0, x0, x1);
+        m1 = fmax3(m1, y0, y1);
+      } else {
+        m2 = fmax3(m2, x0, x1);
+        m3 = fmax3(m3, y0, y1);
+      }
+    }
+  }
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+// P = 2^(S c - m') for one 128-key tile: written to tensor memory as binary16
+// pairs (the lower key in the low half); returns the row sum of the unrounded
+// binary32 P.
+template <bool MASK>
+__device__ __forceinline__ float tile_exp(uint32_t t_s, uint32_t t_p, float c, float neg_m,
+                                          int lim) {
+  const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_m, neg_m);
+  float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t v0[32], v1[32];
+    tmem_ld32x2_wait(t_s + half * 64, t_s + half * 64 + 32, v0, v1);
+    uint32_t p0[16], p1[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      float2 x = make_float2(as_f(v0[e]), as_f(v0[e + 1]));
+      float2 y = make_float2(as_f(v1[e]), as_f(v1[e + 1]));
+      if (MASK) {
+        const int cb = half * 64 + e;
+        if (cb >= lim) x.x = -INFINITY;
+        if (cb + 1 >= lim) x.y = -INFINITY;
+        if (cb + 32 >= lim) y.x = -INFINITY;
+        if (cb + 33 >= lim) y.y = -INFINITY;
+      }
+      const float2 tx = __ffma2_rn(x, c2, nm2);
+      const float2 ty = __ffma2_rn(y, c2, nm2);
+      const float2 ex = make_float2(ex2_approx(tx.x), ex2_approx(tx.y));
+      const float2 ey = make_float2(ex2_approx(ty.x), ex2_approx(ty.y));
+      if (e & 2) {
+        a0 = __fadd2_rn(a0, ex);
+        a1 = __fadd2_rn(a1, ey);
+      } else {
+        a2 = __fadd2_rn(a2, ex);
+        a3 = __fadd2_rn(a3, ey);
+      }
+      p0[e >> 1] = pack_f16x2(ex.x, ex.y);
+      p1[e >> 1] = pack_f16x2(ey.x, ey.y);
+    }
+    tmem_st16(t_p + half * 32, p0);
+    tmem_st16(t_p + half * 32 + 16, p1);
+  }
+  const float2 s01 = __fadd2_rn(a0, a1), s23 = __fadd2_rn(a2, a3);
+  return (s01.x + s01.y) + (s23.x + s23.y);
+}
+
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_vt, const FwdArgs a) {
@@ -200,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kt; ++j) {
-      if (!mbar_wait(BAR(BAR_S_FULL), j & 1, wc)) {
+      if (!mbar_wait_warp(BAR(BAR_S_FULL), j & 1, wc)) {
         ok = false;
         break;
       }
@@ -211,56 +287,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int lim_local = lim - k0;
 
       // pass 1: the row's maximum raw score over the tile
-      float mx = -INFINITY;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v0[32], v1[32];
-        tmem_ld32x2_wait(t_s + half * 64, t_s + half * 64 + 32, v0, v1);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x0 = as_f(v0[e]), x1 = as_f(v1[e]);
-          if (need_mask) {
-            if (half * 64 + e >= lim_local) x0 = -INFINITY;
-            if (half * 64 + 32 + e >= lim_local) x1 = -INFINITY;
-          }
-          mx = fmaxf(mx, fmaxf(x0, x1));
-        }
-      }
+      const float mx = need_mask ? tile_row_max<true>(t_s, lim_local)
+                                 : tile_row_max<false>(t_s, lim_local);
       // c > 0, so max(S) c is the maximum of the scaled scores.
       const float m_new = fmaxf(m, mx * c);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m - m_use);
-      const float neg_m = -m_use;
-
-      // pass 2: P = 2^(S c - m'), the row sum, and P as binary16 into tensor memory
-      float sum = 0.f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v0[32], v1[32];
-        tmem_ld32x2_wait(t_s + half * 64, t_s + half * 64 + 32, v0, v1);
-        uint32_t p0[16], p1[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float x0 = as_f(v0[e]), x1 = as_f(v0[e + 1]);
-          float y0 = as_f(v1[e]), y1 = as_f(v1[e + 1]);
-          if (need_mask) {
-            const int cb = half * 64 + e;
-            if (cb >= lim_local) x0 = -INFINITY;
-            if (cb + 1 >= lim_local) x1 = -INFINITY;
-            if (cb + 32 >= lim_local) y0 = -INFINITY;
-            if (cb + 33 >= lim_local) y1 = -INFINITY;
-          }
-          const float e0 = ex2_approx(fmaf(x0, c, neg_m));
-          const float e1 = ex2_approx(fmaf(x1, c, neg_m));
-          const float f0 = ex2_approx(fmaf(y0, c, neg_m));
-          const float f1 = ex2_approx(fmaf(y1, c, neg_m));
-          sum += (e0 + e1) + (f0 + f1);
-          p0[e >> 1] = pack_f16x2(e0, e1);
-          p1[e >> 1] = pack_f16x2(f0, f1);
-        }
-        tmem_st16(t_p + half * 32, p0);
-        tmem_st16(t_p + half * 32 + 16, p1);
-      }
+      // pass 2: P = 2^(S c - m'), its row sum, and P as binary16 into tensor memory
+      const float sum = need_mask ? tile_exp<true>(t_s, t_p, c, -m_use, lim_local)
+                                  : tile_exp<false>(t_s, t_p, c, -m_use, lim_local);
       l = l * alpha + sum;
       m = m_new;
 

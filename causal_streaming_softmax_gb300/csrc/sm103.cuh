@@ -41,6 +41,13 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Two binary32 values to one binary16x2 word, round to nearest even; `lo`
 // lands in the low 16 bits (the lower column / key).
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -123,6 +130,14 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, w);
+}
+
+// The same wait taken by a whole converged warp: true only if every lane's
+// wait succeeded, so the warp leaves together and never splits around a
+// .sync.aligned tensor-memory instruction.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& w) {
+  const bool ok = mbar_wait(bar, parity, w);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ---------------------------------------------------------------------------
