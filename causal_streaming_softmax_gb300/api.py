@@ -41,7 +41,10 @@ class AttnShape(ctypes.Structure):
 class AttnError(RuntimeError):
     def __init__(self, fn, code):
         self.code = code
-        super().__init__("%s failed: %s (%d)" % (fn, error_string(code), code))
+        msg = "%s failed: %s (%d)" % (fn, error_string(code), code)
+        if code == ATTN_ERR_CUDA:
+            msg += ": " + load_library().attn_last_cuda_error().decode()
+        super().__init__(msg)
 
 
 _lib = None
@@ -72,6 +75,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attn_set_wait_limit_ns.restype = None
     lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.attn_version.restype = ctypes.c_int
+    lib.attn_last_cuda_error.restype = ctypes.c_char_p
     for name in ("attn_fwd", "attn_row_terms", "attn_bwd_keys", "attn_bwd_queries",
                  "attn_last_device_error", "attn_selftest_wait_timeout"):
         getattr(lib, name).restype = ctypes.c_int

@@ -118,6 +118,16 @@ size_t workspace_bytes_for(const Dims& d) {
   return (size_t)d.B * (size_t)(d.kv_count * d.G) * (size_t)d.npairs * kDsTileBytes;
 }
 
+namespace {
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+}
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return ATTN_OK;
+  t_last_cuda_error = e;
+  return ATTN_ERR_CUDA;
+}
+
 bool encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                     uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1) {
   EncodeTiledFn fn = encode_fn();
@@ -139,6 +149,8 @@ using namespace css;
 extern "C" {
 
 int attn_version(void) { return 100; }
+
+const char* attn_last_cuda_error(void) { return cudaGetErrorString(t_last_cuda_error); }
 
 const char* attn_error_string(int code) {
   switch (code) {

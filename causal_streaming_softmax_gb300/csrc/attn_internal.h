@@ -54,6 +54,10 @@ bool aligned16(const void* p);
 bool encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                     uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1);
 
+// ATTN_OK when `e` is cudaSuccess; otherwise records e for
+// attn_last_cuda_error on this host thread and returns ATTN_ERR_CUDA.
+int cuda_status(cudaError_t e);
+
 int launch_fwd(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16_t* k,
                const uint16_t* vt, uint16_t* o, float* lse, cudaStream_t stream);
 int launch_row_terms(const Dims& d, const DevCtx& ctx, const uint16_t* o, const uint16_t* dout,

@@ -12,25 +12,28 @@
 // epilogue writes dK = s * sum (binary32 rows) and dV^T unscaled.
 //
 // GB300 design.
-//   warps 0-7  score gradients, thread = key row (tensor-memory lane); warps
-//              0-3 take queries 0-31 of a step, warps 4-7 queries 32-63
-//   warp 8     TMA producer: K and V^T once, then per step a 64-query tile of
-//              Q and dO and their L and D, through a 4-stage ring
-//   warp 9     MMA issuer
-// K and V are copied once into tensor memory and are the A operands of
-// S^T = K Q^T and dP^T = V dO^T; P^T and dS^T are written to tensor memory
-// and are the A operands of dV += P^T dO and dK += dS^T Q (Q and dO read
-// MN-major from their tiles), so the tensor core reads only the 8 KiB Q / dO
-// tiles from shared memory.  S^T and dP^T are double-buffered: the MMAs of
-// step n+1 run while the score-gradient warps work on step n.  The group's
-// query heads are summed in the tensor-memory accumulators of dK and dV (no
+//   warps 0-7   score gradients, thread = key row (tensor-memory lane); warps
+//               0-3 take queries 0-31 of a step, warps 4-7 queries 32-63
+//   warp 8      TMA producer: K and V^T once, then per step a 64-query tile
+//               of Q and dO and their L and D, through a 4-stage ring
+//   warps 9-12  MMA issuers, one per product chain: S^T, dP^T, dV, dK
+// Every MMA reads its A operand from tensor memory and its B operand (a Q or
+// dO tile, 8 KiB) from shared memory: K and V are copied into tensor memory
+// once; P^T and dS^T are written back over the S^T and dP^T columns they
+// were computed from.  One tcgen05.mma blocks its issuing thread for longer
+// than the tensor core needs for a 128x64x16 product, so the four chains
+// are issued by four warps to keep the tensor core busy.  S^T and dP^T
+// (with P^T and dS^T over them) are double-buffered, so the MMAs of step n+1
+// and the accumulation of step n-1 run while the score-gradient warps work
+// on step n.  dK and dV sum the group's query heads in tensor memory (no
 // atomics, fixed order).  dS^T also goes to shared memory in the
-// 128-byte-swizzled image that the dQ pass reads, and one 16 KiB bulk store
-// per step copies it into the workspace.
+// 128-byte-swizzled image the dQ pass reads, and one 16 KiB bulk store per
+// step copies it into the workspace.
 //
-// Tensor memory (512 columns): K 0-31, V 32-63 (binary16 pairs); S^T / dP^T
-// buffer b at 64+128b / 128+128b (64 columns each); P^T 320-351 and dS^T
-// 352-383 (binary16 pairs); dK 384-447, dV 448-511.
+// Tensor memory (512 columns): K 0-31, V 32-63 (binary16 pairs); buffer b:
+// S^T at 64+128b, dP^T at 128+128b (64 columns each), with P^T of queries
+// 32w..32w+31 over S^T columns 32w..32w+15 and dS^T likewise over dP^T;
+// dK 320-383, dV 384-447.
 #include <math.h>
 
 #include <mutex>
@@ -43,7 +46,7 @@ namespace {
 
 constexpr int kBK = 128;  // keys per CTA
 constexpr int kBQ = 64;   // queries per step
-constexpr int kThreads = 320;
+constexpr int kThreads = 416;
 constexpr int kStages = 4;
 constexpr uint32_t kSmemK = 0;                // K tile: 128 rows x 128 B
 constexpr uint32_t kSmemV = 16384;            // V^T: two 64-key halves of 64 rows x 128 B
@@ -55,24 +58,27 @@ constexpr uint32_t kDSHalf = 16384;           // one 64-query half of a workspac
 constexpr uint32_t kSmemBar = kSmemDS0 + 2 * kDSHalf;
 constexpr uint32_t kSmemBytes = kSmemBar + 256 + 1024;
 
-constexpr uint32_t kColK = 0, kColV = 32, kColS0 = 64, kColPT = 320, kColDST = 352,
-                   kColDK = 384, kColDV = 448;
+constexpr uint32_t kColK = 0, kColV = 32, kColS0 = 64, kColDK = 320, kColDV = 384;
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 64, 0, 0);    // A (tmem) x Q / dO (K-major)
-constexpr uint32_t kIdescAcc = idesc_f16_f32(128, 64, 0, 1);  // A (tmem) x dO / Q (MN-major)
+constexpr uint32_t kIdescAcc = idesc_f16_f32(128, 64, 0, 1);  // P^T / dS^T (tmem) x dO / Q (MN-major)
+
+// Tensor-memory column (within a 64-column S^T or dP^T buffer) of the
+// binary16 pairs of queries 16kk..16kk+15: queries 0-31 sit in columns 0-15
+// and queries 32-63 in columns 32-47 (each warp group writes over what it read).
+__host__ __device__ constexpr uint32_t packed_col(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
 
 enum {
   BAR_KV_FULL = 0,
-  BAR_KV_TMEM,
-  BAR_Q_FULL,
-  BAR_Q_EMPTY = BAR_Q_FULL + kStages,
-  BAR_S_FULL = BAR_Q_EMPTY + kStages,  // [2]
-  BAR_ST_FREE = BAR_S_FULL + 2,        // [2]
-  BAR_P_READY = BAR_ST_FREE + 2,
-  BAR_PT_FREE,
-  BAR_DS_STORED,  // [2]
-  BAR_DONE = BAR_DS_STORED + 2,
+  BAR_KV_TMEM,                          // K and V in tensor memory (256 threads)
+  BAR_Q_FULL,                           // [stage] Q, dO, L, D landed
+  BAR_Q_EMPTY = BAR_Q_FULL + kStages,   // [stage] dV and dK of the step are done (2 commits)
+  BAR_S_FULL = BAR_Q_EMPTY + kStages,   // [2] S^T and dP^T of buffer b are done (2 commits)
+  BAR_P_READY = BAR_S_FULL + 2,         // [2] P^T / dS^T of buffer b written (256 threads)
+  BAR_BUF_FREE = BAR_P_READY + 2,       // [2] dV and dK have read buffer b (2 commits)
+  BAR_DS_STORED = BAR_BUF_FREE + 2,     // [2] the bulk store has read shared dS^T buffer b
+  BAR_DONE = BAR_DS_STORED + 2,         // dK and dV complete (2 commits)
   BAR_COUNT
 };
 static_assert(BAR_COUNT * 8 <= 256, "barrier area");
@@ -129,6 +135,7 @@ __device__ __forceinline__ void score_gradients(const uint32_t (&sv)[32], const 
   }
 }
 
+// 13 warps put four on one scheduler, which caps a thread at 128 registers.
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_keys_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -174,16 +181,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(BAR_KV_TMEM), 256);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(BAR(BAR_Q_FULL + s), 1);
-      mbar_init(BAR(BAR_Q_EMPTY + s), 1);
+      mbar_init(BAR(BAR_Q_EMPTY + s), 2);
     }
     for (int u = 0; u < 2; ++u) {
-      mbar_init(BAR(BAR_S_FULL + u), 1);
-      mbar_init(BAR(BAR_ST_FREE + u), 256);
+      mbar_init(BAR(BAR_S_FULL + u), 2);
+      mbar_init(BAR(BAR_P_READY + u), 256);
+      mbar_init(BAR(BAR_BUF_FREE + u), 2);
       mbar_init(BAR(BAR_DS_STORED + u), 1);
     }
-    mbar_init(BAR(BAR_P_READY), 256);
-    mbar_init(BAR(BAR_PT_FREE), 1);
-    mbar_init(BAR(BAR_DONE), 1);
+    mbar_init(BAR(BAR_DONE), 2);
     fence_mbarrier_init();
   }
   if (warp == 9) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
@@ -225,57 +231,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = (issued > kStages ? issued - kStages : 0); n < issued; ++n)
         drain_wait(BAR(BAR_Q_FULL + n % kStages), (n / kStages) & 1, a.wait_ns);
     }
-  } else if (warp == 9) {
-    // ---------------- MMA issuer (one thread) ----------------
+  } else if (warp >= 9) {
+    // ---------------- MMA issuers: one thread per product chain ----------------
+    const int role = warp - 9;  // 0: S^T = K Q^T, 1: dP^T = V dO^T, 2: dV += P^T dO, 3: dK += dS^T Q
     if (lane == 0 && n_steps > 0) {
-      bool ok = mbar_wait(BAR(BAR_KV_TMEM), 0, wc);
-      tc_fence_after();
-      // dV += P^T dO and dK += dS^T Q of step m (stage m % kStages); the
-      // reduction runs over the step's 64 queries, 16 rows (2 KiB) per K step
-      auto accumulate = [&](int m) -> bool {
-        if (!mbar_wait(BAR(BAR_P_READY), m & 1, wc)) return false;
-        tc_fence_after();
-        const uint32_t st = sbase + kSmemStage0 + (m % kStages) * kStageBytes;
+      bool ok = true;
+      if (role < 2) {
+        ok = mbar_wait(BAR(BAR_KV_TMEM), 0, wc);
+        const uint32_t a_col = role == 0 ? kColK : kColV;
+        const uint32_t b_off = role == 0 ? kStQ : kStDO;
+        for (int n = 0; ok && n < n_steps; ++n) {
+          const int s = n % kStages;
+          const int buf = n & 1;
+          if (!mbar_wait(BAR(BAR_Q_FULL + s), (n / kStages) & 1, wc)) break;
+          if (n >= 2 && !mbar_wait(BAR(BAR_BUF_FREE + buf), ((n >> 1) - 1) & 1, wc)) break;
+          tc_fence_after();
+          const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
+          const uint32_t d = tmem + kColS0 + 128 * buf + 64 * role;
+          // reduction over d: four K=16 steps of 32 B
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + kColDV, tmem + kColPT + kk * 8,
-                 sdesc_sw128(st + kStDO + kk * 2048, 8192, 1024), kIdescAcc,
-                 (m > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + kColDK, tmem + kColDST + kk * 8,
-                 sdesc_sw128(st + kStQ + kk * 2048, 8192, 1024), kIdescAcc,
-                 (m > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(BAR(BAR_Q_EMPTY + m % kStages));
-        mma_commit(BAR(BAR_PT_FREE));
-        return true;
-      };
-      int n = 0;
-      for (; ok && n < n_steps; ++n) {
-        const int s = n % kStages;
-        const int buf = n & 1;
-        if (!mbar_wait(BAR(BAR_Q_FULL + s), (n / kStages) & 1, wc)) break;
-        if (n >= 2 && !mbar_wait(BAR(BAR_ST_FREE + buf), ((n >> 1) - 1) & 1, wc)) break;
-        tc_fence_after();
-        const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
-        const uint32_t c_s = kColS0 + 128 * buf;
-        // S^T = K Q^T and dP^T = V dO^T (reduction over d: four K=16 steps)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + c_s, tmem + kColK + kk * 8, sdesc_sw128(st + kStQ + kk * 32, 16, 1024),
-                 kIdescS, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + c_s + 64, tmem + kColV + kk * 8,
-                 sdesc_sw128(st + kStDO + kk * 32, 16, 1024), kIdescS, kk > 0);
-        mma_commit(BAR(BAR_S_FULL + buf));
-        if (n >= 1 && !accumulate(n - 1)) {
-          ok = false;
-          break;
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(d, tmem + a_col + kk * 8, sdesc_sw128(st + b_off + kk * 32, 16, 1024), kIdescS,
+                   kk > 0);
+          mma_commit(BAR(BAR_S_FULL + buf));
         }
+      } else {
+        const uint32_t d = tmem + (role == 2 ? kColDV : kColDK);
+        const uint32_t b_off = role == 2 ? kStDO : kStQ;
+        for (int n = 0; ok && n < n_steps; ++n) {
+          const int s = n % kStages;
+          const int buf = n & 1;
+          if (!mbar_wait(BAR(BAR_P_READY + buf), (n >> 1) & 1, wc)) break;
+          tc_fence_after();
+          const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
+          // P^T over S^T (dV) or dS^T over dP^T (dK) of buffer b
+          const uint32_t a_base = tmem + kColS0 + 128 * buf + (role == 2 ? 0 : 64);
+          // reduction over the step's 64 queries: 16 rows (2 KiB) of the
+          // MN-major dO / Q tile per K step
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(d, a_base + packed_col(kk), sdesc_sw128(st + b_off + kk * 2048, 8192, 1024),
+                   kIdescAcc, (n > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(BAR(BAR_BUF_FREE + buf));
+          mma_commit(BAR(BAR_Q_EMPTY + s));
+        }
+        mma_commit(BAR(BAR_DONE));
       }
-      if (ok && n == n_steps) accumulate(n_steps - 1);
-      mma_commit(BAR(BAR_DONE));
     }
   } else {
     // ---------------- score gradients: thread = key row ----------------
@@ -332,8 +333,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sv[32], dv[32];
       const uint32_t c_s = kColS0 + 128 * buf + 32 * wg;
       tmem_ld32x2_wait(tmem + lane_base + c_s, tmem + lane_base + c_s + 64, sv, dv);
-      tc_fence_before();
-      mbar_arrive(BAR(BAR_ST_FREE + buf));
 
       const uint8_t* stg = sgen + kSmemStage0 + s * kStageBytes;
       const float4* L4 = reinterpret_cast<const float4*>(stg + kStL) + 8 * wg;
@@ -348,19 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         score_gradients<false>(sv, dv, L4, D4, c, qlo, qhi, pp, dd);
 
-      // P^T / dS^T columns: dV and dK of the previous step have read them
-      if (n >= 1 && !mbar_wait_warp(BAR(BAR_PT_FREE), (n - 1) & 1, wc)) {
-        ok = false;
-        break;
-      }
-      // shared dS^T buffer: the bulk store of step n-2 has read it
+      // shared dS^T buffer b was last filled at step n-2: its bulk store has read it
       if (n >= 2 && !mbar_wait_warp(BAR(BAR_DS_STORED + buf), ((n >> 1) - 1) & 1, wc)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      tmem_st16(tmem + lane_base + kColPT + 16 * wg, pp);
-      tmem_st16(tmem + lane_base + kColDST + 16 * wg, dd);
+      // P^T and dS^T over the S^T / dP^T columns this thread has just read
+      tmem_st16(tmem + lane_base + c_s, pp);
+      tmem_st16(tmem + lane_base + c_s + 64, dd);
       // dS^T row r, queries 32wg..32wg+31 of this 64-query half: chunks 4wg..4wg+3
       const uint32_t dsb = sbase + kSmemDS0 + buf * kDSHalf;
 #pragma unroll
@@ -370,9 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       fence_proxy_async_shared();
-      mbar_arrive(BAR(BAR_P_READY));
+      mbar_arrive(BAR(BAR_P_READY + buf));
       bool stored = true;
-      if (threadIdx.x == 0 && (stored = mbar_wait(BAR(BAR_P_READY), n & 1, wc))) {
+      if (threadIdx.x == 0 && (stored = mbar_wait(BAR(BAR_P_READY + buf), (n >> 1) & 1, wc))) {
         const long long tile = ((long long)b * Hc + h_local0 + g) * d.npairs + d.pair(it, jt);
         bulk_store(a.ws + (size_t)tile * kDsTileBytes + (size_t)hq * kDSHalf, dsb, kDSHalf);
         bulk_commit();
@@ -449,13 +443,15 @@ int launch_bwd_keys(const Dims& d, const DevCtx& ctx, const uint16_t* q, const u
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  std::call_once(attr_once[dev & 63], [] {
-    cudaFuncSetAttribute(bwd_keys_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static cudaError_t attr_status[64];
+  std::call_once(attr_once[dev & 63], [dev] {
+    attr_status[dev & 63] = cudaFuncSetAttribute(bwd_keys_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
+  if (attr_status[dev & 63] != cudaSuccess) return cuda_status(attr_status[dev & 63]);
   KeysArgs args{d, lse, delta, ws, dk, dvt, ctx.err, ctx.wait_ns};
   dim3 grid(d.kv_count, d.nt, d.B);
   bwd_keys_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, args);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return cuda_status(cudaGetLastError());
 }
 
 }  // namespace css

@@ -189,14 +189,16 @@ int launch_bwd_queries(const Dims& d, const DevCtx& ctx, const uint16_t* k, cons
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  std::call_once(attr_once[dev & 63], [] {
-    cudaFuncSetAttribute(bwd_queries_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static cudaError_t attr_status[64];
+  std::call_once(attr_once[dev & 63], [dev] {
+    attr_status[dev & 63] = cudaFuncSetAttribute(bwd_queries_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          kSmemBytes);
   });
+  if (attr_status[dev & 63] != cudaSuccess) return cuda_status(attr_status[dev & 63]);
   QueriesArgs args{d, ws, dq, ctx.err, ctx.wait_ns};
   dim3 grid(d.kv_count * d.G, d.nt, d.B);
   bwd_queries_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tk, args);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return cuda_status(cudaGetLastError());
 }
 
 }  // namespace css

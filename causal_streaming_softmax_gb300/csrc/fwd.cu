@@ -1,5 +1,5 @@
 // fwd.cu - forward pass: causal (or length-masked) attention as a streaming
-// normalised sum, one 128-query tile of one query head per CTA.
+// normalised sum, two 128-query tiles of one query head per CTA.
 //
 // Method (StreamingAttentionSM86.alpha, forward module header and the
 // "one key tile" / epilogue sections): for every key tile up to the
@@ -8,13 +8,20 @@
 // unrounded); O = alpha O + f16(P) V.  Output O / l (binary16, token-major)
 // and L = m + log2 l (binary32).
 //
-// GB300 design (not the pages' SM86 register kernel): warp-specialised CTA
-//   warps 0-3  softmax: one thread per query row (= tensor-memory lane)
-//   warp 4     TMA producer: Q once, then K / V^T tiles through a 2-stage ring
-//   warp 5     MMA issuer: S = Q K^T (SS) and O += P V (P from tensor memory)
-// Tensor memory: S 128 columns (binary32), P 64 columns (binary16 pairs),
-// O 64 columns (binary32): 256 columns, so two CTAs share an SM and one CTA's
-// softmax overlaps the other's MMAs.
+// GB300 design (not the pages' SM86 register kernel).  A CTA takes 256
+// queries of one head as two 128-row tiles, A and B, that share every K/V
+// tile and ping-pong on the exponential unit:
+//   warps 0-3   softmax of tile A, one thread per query row (= TMEM lane)
+//   warps 4-7   softmax of tile B
+//   warp 8      TMA producer: Q once, then K / V^T tiles through a 3-stage ring
+//   warps 9-11  MMA issuers: S_A = Q_A K^T and S_B = Q_B K^T (warp 9),
+//               O_A += P_A V (warp 10), O_B += P_B V (warp 11).  A
+//               tcgen05.mma blocks its issuing thread longer than the tensor
+//               core takes for it, so independent chains get their own warps.
+// Tensor memory (512 columns): S_A 0-127, S_B 128-255 (binary32), P_A
+// 256-319, P_B 320-383 (binary16 pairs), O_A 384-447, O_B 448-511.  Since P
+// has its own columns, S of the next key tile is computed as soon as the
+// softmax has read S, while O += P V of this tile runs.
 #include <math.h>
 
 #include <mutex>
@@ -25,21 +32,21 @@
 namespace css {
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kBN = 128;
-constexpr int kStages = 2;
-constexpr int kThreads = 192;
-constexpr uint32_t kQTileBytes = 128 * 128;        // 128 rows x 128 B
-constexpr uint32_t kStageBytes = 2 * kQTileBytes;  // K tile, then V^T as two 64-key halves
-constexpr uint32_t kSmemQ = 0;
-constexpr uint32_t kSmemStage0 = kQTileBytes;
+constexpr int kBM = 128;   // rows per query tile
+constexpr int kBN = 128;   // keys per key tile
+constexpr int kStages = 3;
+constexpr int kThreads = 384;
+constexpr uint32_t kTileBytes = 128 * 128;         // 128 rows x 128 B
+constexpr uint32_t kStageBytes = 2 * kTileBytes;   // K tile, then V^T as two 64-key halves
+constexpr uint32_t kSmemQ = 0;                     // Q_A, then Q_B
+constexpr uint32_t kSmemStage0 = 2 * kTileBytes;
 constexpr uint32_t kSmemBar = kSmemStage0 + kStages * kStageBytes;
-constexpr uint32_t kSmemBytes = kSmemBar + 128 + 1024;  // barriers + 1024-B alignment slack
+constexpr uint32_t kSmemBytes = kSmemBar + 256 + 1024;  // barriers + 1024-B alignment slack
 
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColP = 128;
-constexpr uint32_t kColO = 192;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0;    // + 128 * tile
+constexpr uint32_t kColP = 256;  // + 64 * tile
+constexpr uint32_t kColO = 384;  // + 64 * tile
+constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);  // Q (K-major) x K (K-major)
 constexpr uint32_t kIdescO = idesc_f16_f32(128, 64, 0, 0);   // P (tmem) x V^T (K-major)
@@ -47,13 +54,15 @@ constexpr uint32_t kIdescO = idesc_f16_f32(128, 64, 0, 0);   // P (tmem) x V^T (
 enum {
   BAR_Q = 0,
   BAR_KV_FULL = 1,
-  BAR_KV_EMPTY = BAR_KV_FULL + kStages,
-  BAR_S_FULL = BAR_KV_EMPTY + kStages,
-  BAR_P_FULL,
-  BAR_O_DONE,
-  BAR_COUNT
+  BAR_KV_EMPTY = BAR_KV_FULL + kStages,  // [stage] both O += P V of the key tile done (2 commits)
+  BAR_S_FULL = BAR_KV_EMPTY + kStages,   // [tile] S of the tile computed
+  BAR_S_FREE = BAR_S_FULL + 2,           // [tile] softmax has read S (128 threads)
+  BAR_P_FULL = BAR_S_FREE + 2,           // [tile] P written and O rescaled (128 threads)
+  BAR_P_FREE = BAR_P_FULL + 2,           // [tile] O += P V done (P may be overwritten)
+  BAR_O_DONE = BAR_P_FREE + 2,           // [tile] every O += P V of the tile done
+  BAR_COUNT = BAR_O_DONE + 2
 };
-static_assert(BAR_COUNT * 8 <= 128, "barrier area");
+static_assert(BAR_COUNT * 8 <= 256, "barrier area");
 
 struct FwdArgs {
   int T, H, Hkv, G, causal;
@@ -74,6 +83,13 @@ static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, ui
   while (!mbar_try_wait(bar, parity))
     if (global_timer_ns() - t0 > limit_ns) return false;
   return true;
+}
+
+// Number of 128-key tiles that query rows [q0, q0 + 128) see.
+__device__ __forceinline__ int key_tiles(int q0, int len, int causal) {
+  if (q0 >= len) return 0;
+  const int kend = causal ? min(len, q0 + kBM) : len;
+  return (kend + kBN - 1) / kBN;
 }
 
 // The row's maximum raw score over one 128-key tile in tensor memory.  MASK
@@ -109,16 +125,20 @@ __device__ __forceinline__ float tile_row_max(uint32_t t_s, int lim) {
 
 // P = 2^(S c - m') for one 128-key tile: written to tensor memory as binary16
 // pairs (the lower key in the low half); returns the row sum of the unrounded
-// binary32 P.
+// binary32 P.  After its last read of S it arrives on `s_free`.
 template <bool MASK>
 __device__ __forceinline__ float tile_exp(uint32_t t_s, uint32_t t_p, float c, float neg_m,
-                                          int lim) {
+                                          int lim, uint32_t s_free) {
   const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_m, neg_m);
   float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     uint32_t v0[32], v1[32];
     tmem_ld32x2_wait(t_s + half * 64, t_s + half * 64 + 32, v0, v1);
+    if (half == 1) {
+      tc_fence_before();
+      mbar_arrive(s_free);
+    }
     uint32_t p0[16], p1[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
@@ -152,7 +172,8 @@ __device__ __forceinline__ float tile_exp(uint32_t t_s, uint32_t t_p, float c, f
   return (s01.x + s01.y) + (s23.x + s23.y);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+// 12 warps: three per scheduler, so up to 168 registers per thread.
+__global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_vt, const FwdArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -166,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.x;
-  const int qt = (int)gridDim.y - 1 - (int)blockIdx.y;  // heaviest causal tiles first
+  const int qb = (int)gridDim.y - 1 - (int)blockIdx.y;  // heaviest causal blocks first
   const int b = blockIdx.z;
   const int kv = h / a.G;
   const int T = a.T;
@@ -175,12 +196,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     len = a.lens[b];
     len = len < 0 ? 0 : (len > T ? T : len);
   }
-  const int q0 = qt * kBM;
-  int n_kt = 0;
-  if (q0 < len) {
-    const int kend = a.causal ? min(len, q0 + kBM) : len;
-    n_kt = (kend + kBN - 1) / kBN;
-  }
+  const int q0 = qb * 2 * kBM;
+  const int n_a = key_tiles(q0, len, a.causal);
+  const int n_b = key_tiles(q0 + kBM, len, a.causal);
+  const int n_kt = max(n_a, n_b);  // key tiles loaded for the two query tiles
 
   WaitCtl wc{a.err, a.wait_ns, &s_abort};
 
@@ -189,20 +208,24 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(BAR(BAR_Q), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(BAR(BAR_KV_FULL + s), 1);
-      mbar_init(BAR(BAR_KV_EMPTY + s), 1);
+      mbar_init(BAR(BAR_KV_EMPTY + s), 2);
     }
-    mbar_init(BAR(BAR_S_FULL), 1);
-    mbar_init(BAR(BAR_P_FULL), 128);
-    mbar_init(BAR(BAR_O_DONE), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(BAR(BAR_S_FULL + t), 1);
+      mbar_init(BAR(BAR_S_FREE + t), 128);
+      mbar_init(BAR(BAR_P_FULL + t), 128);
+      mbar_init(BAR(BAR_P_FREE + t), 1);
+      mbar_init(BAR(BAR_O_DONE + t), 1);
+    }
     fence_mbarrier_init();
   }
-  if (warp == 5) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+  if (warp == 9) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- TMA producer ----------------
     if (lane == 0 && n_kt > 0) {
       tma_prefetch_desc(&tm_q);
@@ -210,8 +233,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       tma_prefetch_desc(&tm_vt);
       const int qplane = b * a.H + h;
       const int kvplane = b * a.Hkv + kv;
-      mbar_arrive_expect_tx(BAR(BAR_Q), kQTileBytes);
-      tma_load_3d(sbase + kSmemQ, &tm_q, BAR(BAR_Q), 0, q0, qplane);
+      // a tile with no visible key is never computed, so its Q is not loaded
+      mbar_arrive_expect_tx(BAR(BAR_Q), ((n_a > 0) + (n_b > 0)) * kTileBytes);
+      if (n_a > 0) tma_load_3d(sbase + kSmemQ, &tm_q, BAR(BAR_Q), 0, q0, qplane);
+      if (n_b > 0) tma_load_3d(sbase + kSmemQ + kTileBytes, &tm_q, BAR(BAR_Q), 0, q0 + kBM, qplane);
       int issued = 0;
       for (int j = 0; j < n_kt; ++j) {
         const int s = j % kStages;
@@ -219,55 +244,85 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
         mbar_arrive_expect_tx(BAR(BAR_KV_FULL + s), kStageBytes);
         tma_load_3d(st, &tm_k, BAR(BAR_KV_FULL + s), 0, j * kBN, kvplane);
-        tma_load_3d(st + kQTileBytes, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN, 0, kvplane);
-        tma_load_3d(st + kQTileBytes + 8192, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN + 64, 0,
+        tma_load_3d(st + kTileBytes, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN, 0, kvplane);
+        tma_load_3d(st + kTileBytes + 8192, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN + 64, 0,
                     kvplane);
         issued = j + 1;
       }
-      // No copy may still be landing when the CTA exits (matters only when a
-      // wait gave up): wait for the last fill of each stage and for Q.
+      // no copy may still be landing when the CTA exits (matters only when a
+      // wait gave up): wait for Q and the last fill of each stage
       drain_wait(BAR(BAR_Q), 0, a.wait_ns);
       for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
         drain_wait(BAR(BAR_KV_FULL + j % kStages), (j / kStages) & 1, a.wait_ns);
     }
-  } else if (warp == 5) {
-    // ---------------- MMA issuer (one thread) ----------------
+  } else if (warp >= 9) {
+    // ---------------- MMA issuers: one thread per product chain ----------------
     if (lane == 0 && n_kt > 0) {
-      const uint32_t q_s = sbase + kSmemQ;
-      bool ok = mbar_wait(BAR(BAR_Q), 0, wc);
-      for (int j = 0; ok && j < n_kt; ++j) {
-        const int s = j % kStages;
-        if (!mbar_wait(BAR(BAR_KV_FULL + s), (j / kStages) & 1, wc)) break;
-        tc_fence_after();
-        const uint32_t k_s = sbase + kSmemStage0 + s * kStageBytes;
-        const uint32_t v_s = k_s + kQTileBytes;
-        // S = Q K^T over d = 64: four K=16 steps inside the 128-byte atom.
+      bool ok = true;
+      if (warp == 9) {
+        // S_A and S_B for each key tile, in that order
+        ok = mbar_wait(BAR(BAR_Q), 0, wc);
+        for (int j = 0; ok && j < n_kt; ++j) {
+          const int s = j % kStages;
+          if (!mbar_wait(BAR(BAR_KV_FULL + s), (j / kStages) & 1, wc)) break;
+          const uint32_t k_s = sbase + kSmemStage0 + s * kStageBytes;
+#pragma unroll 1
+          for (int t = 0; ok && t < 2; ++t) {
+            if (j >= (t ? n_b : n_a)) continue;
+            if (j > 0 && !mbar_wait(BAR(BAR_S_FREE + t), (j - 1) & 1, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t q_s = sbase + kSmemQ + t * kTileBytes;
+            // S = Q K^T over d = 64: four K=16 steps inside the 128-byte atom
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tmem + kColS, sdesc_sw128(q_s + kk * 32, 16, 1024),
-                 sdesc_sw128(k_s + kk * 32, 16, 1024), kIdescS, kk > 0);
-        mma_commit(BAR(BAR_S_FULL));
-        if (!mbar_wait(BAR(BAR_P_FULL), j & 1, wc)) break;
-        tc_fence_after();
-        // O += P V over the tile's 128 keys: eight K=16 steps; keys 0-63 in
-        // the first V^T half, 64-127 in the second.
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(tmem + kColS + 128 * t, sdesc_sw128(q_s + kk * 32, 16, 1024),
+                     sdesc_sw128(k_s + kk * 32, 16, 1024), kIdescS, kk > 0);
+            mma_commit(BAR(BAR_S_FULL + t));
+          }
+        }
+      } else {
+        const int t = warp - 10;
+        const int n_t = t ? n_b : n_a;
+        // walks every loaded key tile so that each stage gets both commits;
+        // for a key tile this query tile does not see, the commit waits until
+        // the tile has been loaded, so that it counts toward that tile's use
+        // of the stage and not toward an earlier one
+        for (int j = 0; ok && j < n_kt; ++j) {
+          const int s = j % kStages;
+          if (j >= n_t) {
+            if (!mbar_wait(BAR(BAR_KV_FULL + s), (j / kStages) & 1, wc)) break;
+          } else {
+            if (!mbar_wait(BAR(BAR_P_FULL + t), j & 1, wc)) break;
+            tc_fence_after();
+            const uint32_t v_s = sbase + kSmemStage0 + s * kStageBytes + kTileBytes;
+            // O += P V over the tile's 128 keys: eight K=16 steps; keys 0-63
+            // in the first V^T half, 64-127 in the second
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + kColO, tmem + kColP + kk * 8,
-                 sdesc_sw128(v_s + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), kIdescO,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(BAR(BAR_KV_EMPTY + s));
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tmem + kColO + 64 * t, tmem + kColP + 64 * t + kk * 8,
+                     sdesc_sw128(v_s + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), kIdescO,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(BAR(BAR_P_FREE + t));
+          }
+          mma_commit(BAR(BAR_KV_EMPTY + s));
+        }
+        mma_commit(BAR(BAR_O_DONE + t));
       }
-      mma_commit(BAR(BAR_O_DONE));
     }
   } else {
-    // ---------------- softmax: thread = query row ----------------
-    const int row = threadIdx.x;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + kColS;
-    const uint32_t t_p = tmem + lane_base + kColP;
-    const uint32_t t_o = tmem + lane_base + kColO;
-    const int qrow = q0 + row;
+    // ---------------- softmax: thread = query row of tile t ----------------
+    const int t = warp >> 2;
+    const int row = threadIdx.x & 127;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + kColS + 128 * t;
+    const uint32_t t_p = tmem + lane_base + kColP + 64 * t;
+    const uint32_t t_o = tmem + lane_base + kColO + 64 * t;
+    const int qt0 = q0 + t * kBM;
+    const int n_t = t ? n_b : n_a;
+    const int qrow = qt0 + row;
     const bool row_ok = qrow < len;
     // keys below `lim` are valid for this row
     int lim = row_ok ? len : 0;
@@ -275,15 +330,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float c = a.c;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kt; ++j) {
-      if (!mbar_wait_warp(BAR(BAR_S_FULL), j & 1, wc)) {
+    for (int j = 0; j < n_t; ++j) {
+      if (!mbar_wait_warp(BAR(BAR_S_FULL + t), j & 1, wc)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const int k0 = j * kBN;
       const bool need_mask =
-          (a.causal && k0 + kBN - 1 > q0) || (k0 + kBN > len) || (q0 + kBM > len);
+          (a.causal && k0 + kBN - 1 > qt0) || (k0 + kBN > len) || (qt0 + kBM > len);
       const int lim_local = lim - k0;
 
       // pass 1: the row's maximum raw score over the tile
@@ -293,36 +348,46 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float m_new = fmaxf(m, mx * c);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m - m_use);
+      // P of the previous tile has been read by its O += P V (and O is final
+      // for the rescale below)
+      if (j > 0 && !mbar_wait_warp(BAR(BAR_P_FREE + t), (j - 1) & 1, wc)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       // pass 2: P = 2^(S c - m'), its row sum, and P as binary16 into tensor memory
-      const float sum = need_mask ? tile_exp<true>(t_s, t_p, c, -m_use, lim_local)
-                                  : tile_exp<false>(t_s, t_p, c, -m_use, lim_local);
+      const float sum = need_mask
+                            ? tile_exp<true>(t_s, t_p, c, -m_use, lim_local, BAR(BAR_S_FREE + t))
+                            : tile_exp<false>(t_s, t_p, c, -m_use, lim_local, BAR(BAR_S_FREE + t));
       l = l * alpha + sum;
       m = m_new;
 
-      // O *= alpha (the previous tile's P V has completed: this tile's S,
-      // committed after it, has).  Skipped for a warp whose rows all keep
-      // their maximum, which leaves O unchanged exactly.
+      // O *= alpha.  Skipped for a warp whose rows all keep their maximum,
+      // which leaves O unchanged exactly.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         uint32_t o0[32], o1[32];
         tmem_ld32x2_wait(t_o, t_o + 32, o0, o1);
+        const float2 al = make_float2(alpha, alpha);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          o0[e] = __float_as_uint(as_f(o0[e]) * alpha);
-          o1[e] = __float_as_uint(as_f(o1[e]) * alpha);
+        for (int e = 0; e < 32; e += 2) {
+          const float2 x = __fmul2_rn(make_float2(as_f(o0[e]), as_f(o0[e + 1])), al);
+          const float2 y = __fmul2_rn(make_float2(as_f(o1[e]), as_f(o1[e + 1])), al);
+          o0[e] = __float_as_uint(x.x), o0[e + 1] = __float_as_uint(x.y);
+          o1[e] = __float_as_uint(y.x), o1[e + 1] = __float_as_uint(y.y);
         }
         tmem_st32(t_o, o0);
         tmem_st32(t_o + 32, o1);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(BAR(BAR_P_FULL));
+      mbar_arrive(BAR(BAR_P_FULL + t));
     }
 
     // ---------------- epilogue: O / l, L = m + log2 l ----------------
     uint16_t* orow = a.o + ((size_t)((size_t)b * T + qrow) * a.H + h) * 64;
     float* lrow = a.lse + ((size_t)b * a.H + h) * T + qrow;
-    if (n_kt > 0) {
-      ok = ok && mbar_wait(BAR(BAR_O_DONE), 0, wc);
+    if (n_t > 0) {
+      ok = ok && mbar_wait_warp(BAR(BAR_O_DONE + t), 0, wc);
       tc_fence_after();
       uint32_t o0[32], o1[32];
       tmem_ld32x2_wait(t_o, t_o + 32, o0, o1);
@@ -356,10 +421,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     // every MMA of this CTA has completed before its tensor memory is freed
-    if (n_kt > 0) drain_wait(BAR(BAR_O_DONE), 0, a.wait_ns);
+    if (n_a > 0) drain_wait(BAR(BAR_O_DONE), 0, a.wait_ns);
+    if (n_b > 0) drain_wait(BAR(BAR_O_DONE + 1), 0, a.wait_ns);
+    if (n_a > 0) drain_wait(BAR(BAR_S_FULL), (n_a - 1) & 1, a.wait_ns);
+    if (n_b > 0) drain_wait(BAR(BAR_S_FULL + 1), (n_b - 1) & 1, a.wait_ns);
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -381,13 +449,15 @@ int launch_fwd(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  std::call_once(attr_once[dev & 63], [] {
-    cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static cudaError_t attr_status[64];
+  std::call_once(attr_once[dev & 63], [dev] {
+    attr_status[dev & 63] = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
+  if (attr_status[dev & 63] != cudaSuccess) return cuda_status(attr_status[dev & 63]);
   FwdArgs args{d.T, d.H, d.Hkv, d.G, d.causal, d.lens, d.c, o, lse, ctx.err, ctx.wait_ns};
-  dim3 grid(d.H, d.nt, d.B);
+  dim3 grid(d.H, (d.T + 2 * kBM - 1) / (2 * kBM), d.B);
   fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, args);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return cuda_status(cudaGetLastError());
 }
 
 }  // namespace css

@@ -94,12 +94,12 @@ int launch_row_terms(const Dims& d, const DevCtx& ctx, const uint16_t* o, const 
   if (blocks > 0x7FFFFFFFll) return ATTN_ERR_SHAPE;
   row_terms_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(o, dout, delta, d.B, d.T, d.H,
                                                                d.lens);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return cuda_status(cudaGetLastError());
 }
 
 int launch_wait_probe(const DevCtx& ctx, uint64_t limit_ns, cudaStream_t stream) {
   wait_probe_kernel<<<1, 32, 0, stream>>>(ctx.err, limit_ns);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return cuda_status(cudaGetLastError());
 }
 
 }  // namespace css

@@ -219,6 +219,13 @@ ATTN_API void attn_set_wait_limit_ns(uint64_t limit_ns);
  */
 ATTN_API int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream);
 
+/*
+ * The CUDA runtime's message for the last CUDA call of this library that
+ * failed on the calling host thread (the cause behind an ATTN_ERR_CUDA), or
+ * "no error".  Diagnostic only.
+ */
+ATTN_API const char* attn_last_cuda_error(void);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 ATTN_API int attn_version(void);
 

@@ -37,6 +37,11 @@ EDGE = [
     (4, 256, 2, 1, False, [63, 64, 65, 200]),
     (3, 384, 4, 2, True, [1, 129, 384]),  # causal with lengths
     (2, 512, 2, 2, True, None),
+    # non-causal lengths where the second 128-row tile of a 256-row block has
+    # no row (it sees no key) while the first sees five key tiles, more than
+    # the forward's K/V stage ring holds
+    (2, 1024, 2, 2, False, [600, 1000]),
+    (1, 1024, 4, 1, True, [600]),
 ]
 
 
