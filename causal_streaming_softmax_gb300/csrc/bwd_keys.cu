@@ -17,6 +17,7 @@
 //   warp 8      TMA producer: K and V^T once, then per step a 64-query tile
 //               of Q and dO and their L and D, through a 4-stage ring
 //   warps 9-12  MMA issuers, one per product chain: S^T, dP^T, dV, dK
+//   warp 13     store: one 16 KiB bulk store of each step's dS^T
 // Every MMA reads its A operand from tensor memory and its B operand (a Q or
 // dO tile, 8 KiB) from shared memory: K and V are copied into tensor memory
 // once; P^T and dS^T are written back over the S^T and dP^T columns they
@@ -27,8 +28,8 @@
 // and the accumulation of step n-1 run while the score-gradient warps work
 // on step n.  dK and dV sum the group's query heads in tensor memory (no
 // atomics, fixed order).  dS^T also goes to shared memory in the
-// 128-byte-swizzled image the dQ pass reads, and one 16 KiB bulk store per
-// step copies it into the workspace.
+// 128-byte-swizzled image the dQ pass reads; the store warp copies it into
+// the workspace, so no score-gradient warp ever waits for a store.
 //
 // Tensor memory (512 columns): K 0-31, V 32-63 (binary16 pairs); buffer b:
 // S^T at 64+128b, dP^T at 128+128b (64 columns each), with P^T of queries
@@ -46,7 +47,7 @@ namespace {
 
 constexpr int kBK = 128;  // keys per CTA
 constexpr int kBQ = 64;   // queries per step
-constexpr int kThreads = 416;
+constexpr int kThreads = 448;
 constexpr int kStages = 4;
 constexpr uint32_t kSmemK = 0;                // K tile: 128 rows x 128 B
 constexpr uint32_t kSmemV = 16384;            // V^T: two 64-key halves of 64 rows x 128 B
@@ -135,7 +136,7 @@ __device__ __forceinline__ void score_gradients(const uint32_t (&sv)[32], const 
   }
 }
 
-// 13 warps put four on one scheduler, which caps a thread at 128 registers.
+// 14 warps put four on a scheduler, which caps a thread at 128 registers.
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_keys_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -231,6 +232,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = (issued > kStages ? issued - kStages : 0); n < issued; ++n)
         drain_wait(BAR(BAR_Q_FULL + n % kStages), (n / kStages) & 1, a.wait_ns);
     }
+  } else if (warp == 13) {
+    // ---------------- store: dS^T of each step into the workspace ----------------
+    if (lane == 0 && n_steps > 0) {
+      const int Hc = d.kv_count * d.G;
+      const int h_local0 = (kv - d.kv_begin) * d.G;
+      for (int n = 0; n < n_steps; ++n) {
+        const int buf = n & 1;
+        // every row of the step's dS^T is in shared memory (and fenced for
+        // the async proxy) once all 256 score-gradient threads arrived
+        if (!mbar_wait(BAR(BAR_P_READY + buf), (n >> 1) & 1, wc)) break;
+        const int g = n / per_g;
+        const int rem = n - g * per_g;
+        const int it = i_lo + (rem >> 1);
+        const int hq = rem & 1;
+        const long long tile = ((long long)b * Hc + h_local0 + g) * d.npairs + d.pair(it, jt);
+        bulk_store(a.ws + (size_t)tile * kDsTileBytes + (size_t)hq * kDSHalf,
+                   sbase + kSmemDS0 + buf * kDSHalf, kDSHalf);
+        bulk_commit();
+        if (n >= 1) {
+          // at most this step's store still reads shared memory: the previous
+          // step's buffer is free for step n + 1
+          bulk_wait_read<1>();
+          mbar_arrive(BAR(BAR_DS_STORED + ((n - 1) & 1)));
+        }
+      }
+      bulk_wait_all<0>();
+    }
   } else if (warp >= 9) {
     // ---------------- MMA issuers: one thread per product chain ----------------
     const int role = warp - 9;  // 0: S^T = K Q^T, 1: dP^T = V dO^T, 2: dV += P^T dO, 3: dK += dS^T Q
@@ -286,8 +314,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = k0 + r;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float c = d.c;
-    const int Hc = d.kv_count * d.G;
-    const int h_local0 = (kv - d.kv_begin) * d.G;
     bool ok = true;
     if (n_steps > 0) {
       // K (warps 0-3) or V (warps 4-7) row r into tensor memory as A operands
@@ -365,24 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       fence_proxy_async_shared();
       mbar_arrive(BAR(BAR_P_READY + buf));
-      bool stored = true;
-      if (threadIdx.x == 0 && (stored = mbar_wait(BAR(BAR_P_READY + buf), (n >> 1) & 1, wc))) {
-        const long long tile = ((long long)b * Hc + h_local0 + g) * d.npairs + d.pair(it, jt);
-        bulk_store(a.ws + (size_t)tile * kDsTileBytes + (size_t)hq * kDSHalf, dsb, kDSHalf);
-        bulk_commit();
-        if (n >= 1) {
-          // at most this step's store still reads shared memory
-          bulk_wait_read<1>();
-          mbar_arrive(BAR(BAR_DS_STORED + ((n - 1) & 1)));
-        }
-      }
-      if (warp == 0) stored = __shfl_sync(0xffffffffu, stored, 0);
-      if (!stored) {
-        ok = false;
-        break;
-      }
     }
-    if (threadIdx.x == 0) bulk_wait_all<0>();
+
+
 
     // ---------------- epilogue: dK = s * sum (rows), dV^T (columns) ----------------
     const bool store = key < T;
