@@ -123,53 +123,50 @@ __device__ __forceinline__ float tile_row_max(uint32_t t_s, int lim) {
   return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
 
-// P = 2^(S c - m') for one 128-key tile: written to tensor memory as binary16
-// pairs (the lower key in the low half); returns the row sum of the unrounded
-// binary32 P.  After its last read of S it arrives on `s_free`.
+// P = 2^(S c - m') for one 128-key tile as binary16 pairs in registers (the
+// lower key in the low half); returns the row sum of the unrounded binary32 P.
+// After its last read of S it arrives on `s_free`.
 template <bool MASK>
-__device__ __forceinline__ float tile_exp(uint32_t t_s, uint32_t t_p, float c, float neg_m,
-                                          int lim, uint32_t s_free) {
+__device__ __forceinline__ float tile_exp(uint32_t t_s, float c, float neg_m, int lim,
+                                          uint32_t s_free, uint32_t (&pk)[64]) {
   const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_m, neg_m);
-  float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+  float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint32_t v0[32], v1[32];
-    tmem_ld32x2_wait(t_s + half * 64, t_s + half * 64 + 32, v0, v1);
-    if (half == 1) {
+  for (int qtr = 0; qtr < 4; ++qtr) {
+    uint32_t v[32];
+    tmem_ld32_wait(t_s + qtr * 32, v);
+    if (qtr == 3) {
       tc_fence_before();
       mbar_arrive(s_free);
     }
-    uint32_t p0[16], p1[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-      float2 x = make_float2(as_f(v0[e]), as_f(v0[e + 1]));
-      float2 y = make_float2(as_f(v1[e]), as_f(v1[e + 1]));
+      float2 x = make_float2(as_f(v[e]), as_f(v[e + 1]));
       if (MASK) {
-        const int cb = half * 64 + e;
+        const int cb = qtr * 32 + e;
         if (cb >= lim) x.x = -INFINITY;
         if (cb + 1 >= lim) x.y = -INFINITY;
-        if (cb + 32 >= lim) y.x = -INFINITY;
-        if (cb + 33 >= lim) y.y = -INFINITY;
       }
       const float2 tx = __ffma2_rn(x, c2, nm2);
-      const float2 ty = __ffma2_rn(y, c2, nm2);
       const float2 ex = make_float2(ex2_approx(tx.x), ex2_approx(tx.y));
-      const float2 ey = make_float2(ex2_approx(ty.x), ex2_approx(ty.y));
-      if (e & 2) {
+      if (e & 2)
         a0 = __fadd2_rn(a0, ex);
-        a1 = __fadd2_rn(a1, ey);
-      } else {
-        a2 = __fadd2_rn(a2, ex);
-        a3 = __fadd2_rn(a3, ey);
-      }
-      p0[e >> 1] = pack_f16x2(ex.x, ex.y);
-      p1[e >> 1] = pack_f16x2(ey.x, ey.y);
+      else
+        a1 = __fadd2_rn(a1, ex);
+      // key k of the tile goes to packed word k / 2
+      pk[qtr * 16 + (e >> 1)] = pack_f16x2(ex.x, ex.y);
     }
-    tmem_st16(t_p + half * 32, p0);
-    tmem_st16(t_p + half * 32 + 16, p1);
   }
-  const float2 s01 = __fadd2_rn(a0, a1), s23 = __fadd2_rn(a2, a3);
-  return (s01.x + s01.y) + (s23.x + s23.y);
+  const float2 s01 = __fadd2_rn(a0, a1);
+  return s01.x + s01.y;
+}
+
+// Stores the 64 packed words of P (128 keys) into the row's P columns.
+__device__ __forceinline__ void store_p(uint32_t t_p, const uint32_t (&pk)[64]) {
+  const uint32_t(&w0)[32] = *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]);
+  const uint32_t(&w1)[32] = *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]);
+  tmem_st32(t_p, w0);
+  tmem_st32(t_p + 32, w1);
 }
 
 // 12 warps: three per scheduler, so up to 168 registers per thread.
@@ -348,17 +345,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = fmaxf(m, mx * c);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m - m_use);
+      // pass 2: P = 2^(S c - m') and its row sum, P kept in registers
+      uint32_t pk[64];
+      const float sum = need_mask
+                            ? tile_exp<true>(t_s, c, -m_use, lim_local, BAR(BAR_S_FREE + t), pk)
+                            : tile_exp<false>(t_s, c, -m_use, lim_local, BAR(BAR_S_FREE + t), pk);
       // P of the previous tile has been read by its O += P V (and O is final
-      // for the rescale below)
+      // for the rescale below): only now is P overwritten
       if (j > 0 && !mbar_wait_warp(BAR(BAR_P_FREE + t), (j - 1) & 1, wc)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // pass 2: P = 2^(S c - m'), its row sum, and P as binary16 into tensor memory
-      const float sum = need_mask
-                            ? tile_exp<true>(t_s, t_p, c, -m_use, lim_local, BAR(BAR_S_FREE + t))
-                            : tile_exp<false>(t_s, t_p, c, -m_use, lim_local, BAR(BAR_S_FREE + t));
+      store_p(t_p, pk);
       l = l * alpha + sum;
       m = m_new;
 
