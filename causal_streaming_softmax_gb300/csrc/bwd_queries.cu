@@ -9,7 +9,7 @@
 //
 // GB300 design: warp 4 copies each workspace tile (32 KiB, already in the
 // shared-memory image the tensor core reads) with one bulk copy and K's tile
-// with TMA, through a 4-stage ring; warp 5 issues dQ += dS K with dS as an
+// with TMA, through a 2-stage ring (two CTAs per SM); warp 5 issues dQ += dS K with dS as an
 // MN-major A operand (queries along the 128-byte rows) and K as an MN-major
 // B operand; warps 0-3 scale and store.  The pass is bound by reading dS
 // from HBM.
@@ -26,7 +26,7 @@ namespace {
 constexpr int kBM = 128;  // queries per CTA
 constexpr int kBN = 128;  // keys per tile
 constexpr int kThreads = 192;
-constexpr int kStages = 4;
+constexpr int kStages = 2;  // two CTAs share an SM: one's epilogue overlaps the other's loads
 constexpr uint32_t kKTileBytes = 16384;
 constexpr uint32_t kStageBytes = kDsTileBytes + kKTileBytes;  // dS^T image, then K tile
 constexpr uint32_t kSmemBar = kStages * kStageBytes;
@@ -54,7 +54,7 @@ static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, ui
   return true;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     bwd_queries_kernel(const __grid_constant__ CUtensorMap tm_k, const QueriesArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
