@@ -76,6 +76,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.attn_version.restype = ctypes.c_int
     lib.attn_last_cuda_error.restype = ctypes.c_char_p
+    lib.attn_selftest_arith.argtypes = [vp, vp, vp, ctypes.c_int, vp]
+    lib.attn_selftest_arith.restype = ctypes.c_int
     for name in ("attn_fwd", "attn_row_terms", "attn_bwd_keys", "attn_bwd_queries",
                  "attn_last_device_error", "attn_selftest_wait_timeout"):
         getattr(lib, name).restype = ctypes.c_int
@@ -223,6 +225,19 @@ def check_device_error(stream=None) -> None:
 
 def set_wait_limit_ns(ns: int) -> None:
     load_library().attn_set_wait_limit_ns(int(ns))
+
+
+def selftest_arith(x, stream=None):
+    """Runs the library's binary16 packing and exponential over the float32
+    CUDA tensor x (even length): returns (packed uint32 words, 2^x)."""
+    if not (x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()):
+        raise TypeError("x must be a contiguous float32 CUDA tensor")
+    n = x.numel()
+    packed = torch.empty(n // 2, dtype=torch.int32, device=x.device)
+    e2 = torch.empty(n, dtype=torch.float32, device=x.device)
+    _check("attn_selftest_arith", load_library().attn_selftest_arith(
+        x.data_ptr(), packed.data_ptr(), e2.data_ptr(), n, _stream_ptr(stream)))
+    return packed, e2
 
 
 def selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None) -> int:

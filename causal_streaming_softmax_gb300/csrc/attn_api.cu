@@ -248,6 +248,17 @@ int attn_last_device_error(void* stream) {
   return ATTN_ERR_DEVICE_TIMEOUT;
 }
 
+int attn_selftest_arith(const float* x, uint32_t* packed, float* e2, int n, void* stream) {
+  if (n < 0 || (n & 1)) return ATTN_ERR_SHAPE;
+  if (n > 0 && (!x || !packed || !e2)) return ATTN_ERR_NULL;
+  DevCtx ctx;
+  int rc = device_context(&ctx);
+  if (rc != ATTN_OK) return rc;
+  rc = launch_arith_probe(x, packed, e2, n, static_cast<cudaStream_t>(stream));
+  if (rc != ATTN_OK) return rc;
+  return cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+}
+
 int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   DevCtx ctx;
   int rc = device_context(&ctx);

@@ -69,5 +69,6 @@ int launch_bwd_keys(const Dims& d, const DevCtx& ctx, const uint16_t* q, const u
 int launch_bwd_queries(const Dims& d, const DevCtx& ctx, const uint16_t* k, const uint8_t* ws,
                        float* dq, cudaStream_t stream);
 int launch_wait_probe(const DevCtx& ctx, uint64_t limit_ns, cudaStream_t stream);
+int launch_arith_probe(const float* x, uint32_t* packed, float* e2, int n, cudaStream_t stream);
 
 }  // namespace css

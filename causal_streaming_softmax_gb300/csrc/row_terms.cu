@@ -84,7 +84,21 @@ __global__ void wait_probe_kernel(uint32_t* err, uint64_t limit_ns) {
   __syncthreads();
 }
 
+// The binary16 packing and the exponential exactly as the kernels use them.
+__global__ void arith_probe_kernel(const float* __restrict__ x, uint32_t* __restrict__ packed,
+                                   float* __restrict__ e2, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) e2[i] = ex2_approx(x[i]);
+  if (2 * i + 1 < n) packed[i] = pack_f16x2(x[2 * i], x[2 * i + 1]);
+}
+
 }  // namespace
+
+int launch_arith_probe(const float* x, uint32_t* packed, float* e2, int n, cudaStream_t stream) {
+  if (n <= 0) return ATTN_OK;
+  arith_probe_kernel<<<(n + 255) / 256, 256, 0, stream>>>(x, packed, e2, n);
+  return cuda_status(cudaGetLastError());
+}
 
 int launch_row_terms(const Dims& d, const DevCtx& ctx, const uint16_t* o, const uint16_t* dout,
                      float* delta, cudaStream_t stream) {

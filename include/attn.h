@@ -226,6 +226,17 @@ ATTN_API int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream);
  */
 ATTN_API const char* attn_last_cuda_error(void);
 
+/*
+ * Self-test of the two arithmetic steps every kernel relies on (the
+ * precision contract of the forward module header: P rounded to binary16
+ * before its product with V, and P = 2^t): for device arrays x[n] (n even),
+ * writes packed[i] = the binary16x2 word of (x[2i] low, x[2i+1] high),
+ * rounded to nearest even, and e2[i] = 2^x[i] as the kernels compute it.
+ * Synchronises the stream.  Not part of the method; for tests.
+ */
+ATTN_API int attn_selftest_arith(const float* x, uint32_t* packed, float* e2, int n,
+                                 void* stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 ATTN_API int attn_version(void);
 
