@@ -20,21 +20,20 @@
 //   warp 13     store: one 16 KiB bulk store of each step's dS^T
 // Every MMA reads its A operand from tensor memory and its B operand (a Q or
 // dO tile, 8 KiB) from shared memory: K and V are copied into tensor memory
-// once; P^T and dS^T are written back over the S^T and dP^T columns they
-// were computed from.  One tcgen05.mma blocks its issuing thread for longer
-// than the tensor core needs for a 128x64x16 product, so the four chains
-// are issued by four warps to keep the tensor core busy.  S^T and dP^T
-// (with P^T and dS^T over them) are double-buffered, so the MMAs of step n+1
-// and the accumulation of step n-1 run while the score-gradient warps work
-// on step n.  dK and dV sum the group's query heads in tensor memory (no
-// atomics, fixed order).  dS^T also goes to shared memory in the
-// 128-byte-swizzled image the dQ pass reads; the store warp copies it into
-// the workspace, so no score-gradient warp ever waits for a store.
+// once.  The score-gradient warps load a step's S^T and dP^T into registers
+// and release the buffer at once, so the next step's S^T and dP^T run while
+// they compute; they write P^T and dS^T as binary16 pairs into one of two
+// separate buffers, which dV and dK read, so the accumulation of a step has
+// two steps to finish.  With those latencies off the loop, a step costs the
+// score-gradient work.  The four product chains are issued by four warps.
+// dK and dV sum the group's query heads in tensor memory (no atomics, fixed
+// order).  dS^T also goes to shared memory in the 128-byte-swizzled image
+// the dQ pass reads; the store warp copies it into the workspace, so no
+// score-gradient warp ever waits for a store.
 //
-// Tensor memory (512 columns): K 0-31, V 32-63 (binary16 pairs); buffer b:
-// S^T at 64+128b, dP^T at 128+128b (64 columns each), with P^T of queries
-// 32w..32w+31 over S^T columns 32w..32w+15 and dS^T likewise over dP^T;
-// dK 320-383, dV 384-447.
+// Tensor memory (512 columns): K 0-31, V 32-63 (binary16 pairs), S^T 64-127,
+// dP^T 128-191; pair buffer b at 192+64b: P^T of queries 32w..32w+31 at
+// 16w..16w+15, dS^T likewise at 32+16w; dK 320-383, dV 384-447.
 #include <math.h>
 
 #include <mutex>
@@ -56,30 +55,32 @@ constexpr uint32_t kStQ = 0, kStDO = 8192, kStL = 16384, kStD = 16640;
 constexpr uint32_t kStageBytes = 17408;       // a multiple of 1024
 constexpr uint32_t kSmemDS0 = kSmemStage0 + kStages * kStageBytes;
 constexpr uint32_t kDSHalf = 16384;           // one 64-query half of a workspace tile
-constexpr uint32_t kSmemBar = kSmemDS0 + 2 * kDSHalf;
+constexpr int kDSBufs = 3;                    // shared dS^T staging buffers
+constexpr uint32_t kSmemBar = kSmemDS0 + kDSBufs * kDSHalf;
 constexpr uint32_t kSmemBytes = kSmemBar + 256 + 1024;
 
-constexpr uint32_t kColK = 0, kColV = 32, kColS0 = 64, kColDK = 320, kColDV = 384;
+constexpr uint32_t kColK = 0, kColV = 32, kColS = 64, kColDP = 128, kColPK = 192;
+constexpr uint32_t kColDK = 320, kColDV = 384;
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 64, 0, 0);    // A (tmem) x Q / dO (K-major)
 constexpr uint32_t kIdescAcc = idesc_f16_f32(128, 64, 0, 1);  // P^T / dS^T (tmem) x dO / Q (MN-major)
 
-// Tensor-memory column (within a 64-column S^T or dP^T buffer) of the
-// binary16 pairs of queries 16kk..16kk+15: queries 0-31 sit in columns 0-15
-// and queries 32-63 in columns 32-47 (each warp group writes over what it read).
-__host__ __device__ constexpr uint32_t packed_col(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
+// Tensor-memory column (within the 32 P^T or dS^T columns of a pair buffer)
+// of the binary16 pairs of queries 16kk..16kk+15.
+__host__ __device__ constexpr uint32_t packed_col(int kk) { return 8 * kk; }
 
 enum {
   BAR_KV_FULL = 0,
   BAR_KV_TMEM,                          // K and V in tensor memory (256 threads)
   BAR_Q_FULL,                           // [stage] Q, dO, L, D landed
   BAR_Q_EMPTY = BAR_Q_FULL + kStages,   // [stage] dV and dK of the step are done (2 commits)
-  BAR_S_FULL = BAR_Q_EMPTY + kStages,   // [2] S^T and dP^T of buffer b are done (2 commits)
-  BAR_P_READY = BAR_S_FULL + 2,         // [2] P^T / dS^T of buffer b written (256 threads)
-  BAR_BUF_FREE = BAR_P_READY + 2,       // [2] dV and dK have read buffer b (2 commits)
-  BAR_DS_STORED = BAR_BUF_FREE + 2,     // [2] the bulk store has read shared dS^T buffer b
-  BAR_DONE = BAR_DS_STORED + 2,         // dK and dV complete (2 commits)
+  BAR_S_FULL = BAR_Q_EMPTY + kStages,   // S^T and dP^T of the step are done (2 commits)
+  BAR_LOADED,                           // S^T and dP^T are in registers (256 threads)
+  BAR_P_READY,                          // [2] P^T / dS^T of pair buffer b written (256 threads)
+  BAR_PK_FREE = BAR_P_READY + 2,        // [2] dV and dK have read pair buffer b (2 commits)
+  BAR_DS_STORED = BAR_PK_FREE + 2,      // [3] the bulk store has read shared dS^T buffer b
+  BAR_DONE = BAR_DS_STORED + kDSBufs,   // dK and dV complete (2 commits)
   BAR_COUNT
 };
 static_assert(BAR_COUNT * 8 <= 256, "barrier area");
@@ -104,33 +105,47 @@ static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, ui
   return true;
 }
 
-// Score gradients of 32 queries for one key row: P = 2^(S c - L),
-// dS = P (dP - D), both packed to binary16 pairs.  MASK zeroes the entries
-// outside [qlo, qhi) (local query indices).
+// Probabilities of 32 queries for one key row: P = 2^(S c - L), kept in
+// binary32 for dS and packed to binary16 pairs for dV.  MASK zeroes the
+// entries outside [qlo, qhi) (local query indices).
 template <bool MASK>
-__device__ __forceinline__ void score_gradients(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
-                                                const float4* __restrict__ L4,
-                                                const float4* __restrict__ D4, float c, int qlo,
-                                                int qhi, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
+__device__ __forceinline__ void probabilities(const uint32_t (&sv)[32],
+                                              const float4* __restrict__ L4, float c, int qlo,
+                                              int qhi, float2 (&p)[16], uint32_t (&pp)[16]) {
   const float2 c2 = make_float2(c, c);
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
     const float4 l = L4[u];
-    const float4 dl = D4[u];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int e = 4 * u + 2 * h;
       const float2 nl = h ? make_float2(-l.z, -l.w) : make_float2(-l.x, -l.y);
-      const float2 nd = h ? make_float2(-dl.z, -dl.w) : make_float2(-dl.x, -dl.y);
       const float2 t = __ffma2_rn(make_float2(as_f(sv[e]), as_f(sv[e + 1])), c2, nl);
-      float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-      const float2 g = __fadd2_rn(make_float2(as_f(dv[e]), as_f(dv[e + 1])), nd);
-      float2 ds = __fmul2_rn(p, g);
+      float2 q = make_float2(ex2_approx(t.x), ex2_approx(t.y));
       if (MASK) {
-        if (e < qlo || e >= qhi) p.x = 0.f, ds.x = 0.f;
-        if (e + 1 < qlo || e + 1 >= qhi) p.y = 0.f, ds.y = 0.f;
+        if (e < qlo || e >= qhi) q.x = 0.f;
+        if (e + 1 < qlo || e + 1 >= qhi) q.y = 0.f;
       }
-      pp[e >> 1] = pack_f16x2(p.x, p.y);
+      p[e >> 1] = q;
+      pp[e >> 1] = pack_f16x2(q.x, q.y);
+    }
+  }
+}
+
+// Score gradients dS = P (dP - D) of the same 32 queries, packed to binary16
+// pairs (a masked P is zero, so is its dS).
+__device__ __forceinline__ void score_gradients(const float2 (&p)[16], const uint32_t (&dv)[32],
+                                                const float4* __restrict__ D4,
+                                                uint32_t (&dd)[16]) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const float4 dl = D4[u];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = 4 * u + 2 * h;
+      const float2 nd = h ? make_float2(-dl.z, -dl.w) : make_float2(-dl.x, -dl.y);
+      const float2 g = __fadd2_rn(make_float2(as_f(dv[e]), as_f(dv[e + 1])), nd);
+      const float2 ds = __fmul2_rn(p[e >> 1], g);
       dd[e >> 1] = pack_f16x2(ds.x, ds.y);
     }
   }
@@ -184,12 +199,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(BAR_Q_FULL + s), 1);
       mbar_init(BAR(BAR_Q_EMPTY + s), 2);
     }
+    mbar_init(BAR(BAR_S_FULL), 2);
+    mbar_init(BAR(BAR_LOADED), 256);
     for (int u = 0; u < 2; ++u) {
-      mbar_init(BAR(BAR_S_FULL + u), 2);
       mbar_init(BAR(BAR_P_READY + u), 256);
-      mbar_init(BAR(BAR_BUF_FREE + u), 2);
-      mbar_init(BAR(BAR_DS_STORED + u), 1);
+      mbar_init(BAR(BAR_PK_FREE + u), 2);
     }
+    for (int u = 0; u < kDSBufs; ++u) mbar_init(BAR(BAR_DS_STORED + u), 1);
     mbar_init(BAR(BAR_DONE), 2);
     fence_mbarrier_init();
   }
@@ -211,12 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sbase + kSmemK, &tm_k, BAR(BAR_KV_FULL), 0, k0, kvplane);
       tma_load_3d(sbase + kSmemV, &tm_vt, BAR(BAR_KV_FULL), k0, 0, kvplane);
       tma_load_3d(sbase + kSmemV + 8192, &tm_vt, BAR(BAR_KV_FULL), k0 + 64, 0, kvplane);
-      int issued = 0;
+      int issued = 0, g = 0, rem = 0;
       for (int n = 0; n < n_steps; ++n) {
         const int s = n % kStages;
         if (n >= kStages && !mbar_wait(BAR(BAR_Q_EMPTY + s), ((n / kStages) - 1) & 1, wc)) break;
-        const int g = n / per_g;
-        const int rem = n - g * per_g;
         const int q0 = (i_lo + (rem >> 1)) * kTile + (rem & 1) * kBQ;
         const int qplane = b * d.H + kv * d.G + g;
         const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
@@ -227,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(st + kStL, a.lse + lo, kBQ * 4, BAR(BAR_Q_FULL + s));
         bulk_load(st + kStD, a.delta + lo, kBQ * 4, BAR(BAR_Q_FULL + s));
         issued = n + 1;
+        if (++rem == per_g) rem = 0, ++g;
       }
       drain_wait(BAR(BAR_KV_FULL), 0, a.wait_ns);
       for (int n = (issued > kStages ? issued - kStages : 0); n < issued; ++n)
@@ -237,24 +252,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_steps > 0) {
       const int Hc = d.kv_count * d.G;
       const int h_local0 = (kv - d.kv_begin) * d.G;
+      int g = 0, rem = 0;
       for (int n = 0; n < n_steps; ++n) {
-        const int buf = n & 1;
         // every row of the step's dS^T is in shared memory (and fenced for
         // the async proxy) once all 256 score-gradient threads arrived
-        if (!mbar_wait(BAR(BAR_P_READY + buf), (n >> 1) & 1, wc)) break;
-        const int g = n / per_g;
-        const int rem = n - g * per_g;
+        if (!mbar_wait(BAR(BAR_P_READY + (n & 1)), (n >> 1) & 1, wc)) break;
         const int it = i_lo + (rem >> 1);
         const int hq = rem & 1;
         const long long tile = ((long long)b * Hc + h_local0 + g) * d.npairs + d.pair(it, jt);
+        if (++rem == per_g) rem = 0, ++g;
         bulk_store(a.ws + (size_t)tile * kDsTileBytes + (size_t)hq * kDSHalf,
-                   sbase + kSmemDS0 + buf * kDSHalf, kDSHalf);
+                   sbase + kSmemDS0 + (n % kDSBufs) * kDSHalf, kDSHalf);
         bulk_commit();
         if (n >= 1) {
           // at most this step's store still reads shared memory: the previous
-          // step's buffer is free for step n + 1
+          // step's buffer is free for step n + 2
           bulk_wait_read<1>();
-          mbar_arrive(BAR(BAR_DS_STORED + ((n - 1) & 1)));
+          mbar_arrive(BAR(BAR_DS_STORED + (n - 1) % kDSBufs));
         }
       }
       bulk_wait_all<0>();
@@ -268,39 +282,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(BAR(BAR_KV_TMEM), 0, wc);
         const uint32_t a_col = role == 0 ? kColK : kColV;
         const uint32_t b_off = role == 0 ? kStQ : kStDO;
+        const uint32_t d = tmem + (role == 0 ? kColS : kColDP);
         for (int n = 0; ok && n < n_steps; ++n) {
           const int s = n % kStages;
-          const int buf = n & 1;
           if (!mbar_wait(BAR(BAR_Q_FULL + s), (n / kStages) & 1, wc)) break;
-          if (n >= 2 && !mbar_wait(BAR(BAR_BUF_FREE + buf), ((n >> 1) - 1) & 1, wc)) break;
+          // the score-gradient warps hold step n-1's S^T and dP^T in registers
+          if (n >= 1 && !mbar_wait(BAR(BAR_LOADED), (n - 1) & 1, wc)) break;
           tc_fence_after();
           const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
-          const uint32_t d = tmem + kColS0 + 128 * buf + 64 * role;
           // reduction over d: four K=16 steps of 32 B
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ts(d, tmem + a_col + kk * 8, sdesc_sw128(st + b_off + kk * 32, 16, 1024), kIdescS,
                    kk > 0);
-          mma_commit(BAR(BAR_S_FULL + buf));
+          mma_commit(BAR(BAR_S_FULL));
         }
       } else {
         const uint32_t d = tmem + (role == 2 ? kColDV : kColDK);
         const uint32_t b_off = role == 2 ? kStDO : kStQ;
         for (int n = 0; ok && n < n_steps; ++n) {
           const int s = n % kStages;
-          const int buf = n & 1;
-          if (!mbar_wait(BAR(BAR_P_READY + buf), (n >> 1) & 1, wc)) break;
+          const int pb = n & 1;
+          if (!mbar_wait(BAR(BAR_P_READY + pb), (n >> 1) & 1, wc)) break;
           tc_fence_after();
           const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
-          // P^T over S^T (dV) or dS^T over dP^T (dK) of buffer b
-          const uint32_t a_base = tmem + kColS0 + 128 * buf + (role == 2 ? 0 : 64);
+          // P^T (dV) or dS^T (dK) of pair buffer pb
+          const uint32_t a_base = tmem + kColPK + 64 * pb + (role == 2 ? 0 : 32);
           // reduction over the step's 64 queries: 16 rows (2 KiB) of the
           // MN-major dO / Q tile per K step
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ts(d, a_base + packed_col(kk), sdesc_sw128(st + b_off + kk * 2048, 8192, 1024),
                    kIdescAcc, (n > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(BAR(BAR_BUF_FREE + buf));
+          mma_commit(BAR(BAR_PK_FREE + pb));
           mma_commit(BAR(BAR_Q_EMPTY + s));
         }
         mma_commit(BAR(BAR_DONE));
@@ -343,22 +357,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(BAR(BAR_KV_TMEM));
     }
+    int rem_c = 0;
     for (int n = 0; ok && n < n_steps; ++n) {
       const int s = n % kStages;
-      const int buf = n & 1;
-      const int g = n / per_g;
-      const int rem = n - g * per_g;
+      const int pb = n & 1;
+      const int rem = rem_c;
+      if (++rem_c == per_g) rem_c = 0;
       const int it = i_lo + (rem >> 1);
       const int hq = rem & 1;
       const int qb = it * kTile + hq * kBQ + 32 * wg;  // this thread's first query
-      if (!mbar_wait_warp(BAR(BAR_S_FULL + buf), (n >> 1) & 1, wc)) {
+      if (!mbar_wait_warp(BAR(BAR_S_FULL), n & 1, wc)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      // this thread's S^T and dP^T columns into registers, then the buffer
+      // is free for the next step's products
       uint32_t sv[32], dv[32];
-      const uint32_t c_s = kColS0 + 128 * buf + 32 * wg;
-      tmem_ld32x2_wait(tmem + lane_base + c_s, tmem + lane_base + c_s + 64, sv, dv);
+      tmem_ld32x2_wait(tmem + lane_base + kColS + 32 * wg, tmem + lane_base + kColDP + 32 * wg,
+                       sv, dv);
+      tc_fence_before();
+      mbar_arrive(BAR(BAR_LOADED));
 
       const uint8_t* stg = sgen + kSmemStage0 + s * kStageBytes;
       const float4* L4 = reinterpret_cast<const float4*>(stg + kStL) + 8 * wg;
@@ -367,22 +386,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           (d.causal && qb < k0 + kBK - 1) || (qb + 32 > len) || (k0 + kBK > len);
       const int qlo = (d.causal ? key : 0) - qb;
       const int qhi = (key < len ? len : 0) - qb;
+      float2 p[16];
       uint32_t pp[16], dd[16];
       if (need_mask)
-        score_gradients<true>(sv, dv, L4, D4, c, qlo, qhi, pp, dd);
+        probabilities<true>(sv, L4, c, qlo, qhi, p, pp);
       else
-        score_gradients<false>(sv, dv, L4, D4, c, qlo, qhi, pp, dd);
-
-      // shared dS^T buffer b was last filled at step n-2: its bulk store has read it
-      if (n >= 2 && !mbar_wait_warp(BAR(BAR_DS_STORED + buf), ((n >> 1) - 1) & 1, wc)) {
+        probabilities<false>(sv, L4, c, qlo, qhi, p, pp);
+      score_gradients(p, dv, D4, dd);
+      // pair buffer pb was last read by dV and dK of step n-2
+      if (n >= 2 && !mbar_wait_warp(BAR(BAR_PK_FREE + pb), ((n >> 1) - 1) & 1, wc)) {
         ok = false;
         break;
       }
-      // P^T and dS^T over the S^T / dP^T columns this thread has just read
-      tmem_st16(tmem + lane_base + c_s, pp);
-      tmem_st16(tmem + lane_base + c_s + 64, dd);
+      tc_fence_after();
+      const uint32_t pk = kColPK + 64 * pb + 16 * wg;
+      tmem_st16(tmem + lane_base + pk, pp);
+      tmem_st16(tmem + lane_base + pk + 32, dd);
+
+      // shared dS^T buffer n % 3 was last filled at step n-3: its bulk store has read it
+      const int dsbuf = n % kDSBufs;
+      if (n >= kDSBufs &&
+          !mbar_wait_warp(BAR(BAR_DS_STORED + dsbuf), ((n / kDSBufs) - 1) & 1, wc)) {
+        ok = false;
+        break;
+      }
       // dS^T row r, queries 32wg..32wg+31 of this 64-query half: chunks 4wg..4wg+3
-      const uint32_t dsb = sbase + kSmemDS0 + buf * kDSHalf;
+      const uint32_t dsb = sbase + kSmemDS0 + dsbuf * kDSHalf;
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         st_shared_v4(dsb + sw128_offset(r, 4 * wg + u), dd[4 * u], dd[4 * u + 1], dd[4 * u + 2],
@@ -390,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       fence_proxy_async_shared();
-      mbar_arrive(BAR(BAR_P_READY + buf));
+      mbar_arrive(BAR(BAR_P_READY + pb));
     }
 
 
