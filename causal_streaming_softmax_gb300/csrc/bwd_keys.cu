@@ -15,7 +15,7 @@
 //   warps 0-7   score gradients, thread = key row (tensor-memory lane); warps
 //               0-3 take queries 0-31 of a step, warps 4-7 queries 32-63
 //   warp 8      TMA producer: K and V^T once, then per step a 64-query tile
-//               of Q and dO and their L and D, through a 4-stage ring
+//               of Q and dO and their L and D, through an 8-stage ring
 //   warps 9-12  MMA issuers, one per product chain: S^T, dP^T, dV, dK
 //   warp 13     store: one 16 KiB bulk store of each step's dS^T
 // Every MMA reads its A operand from tensor memory and its B operand (a Q or
@@ -47,7 +47,7 @@ namespace {
 constexpr int kBK = 128;  // keys per CTA
 constexpr int kBQ = 64;   // queries per step
 constexpr int kThreads = 448;
-constexpr int kStages = 4;
+constexpr int kStages = 8;
 constexpr uint32_t kSmemK = 0;                // K tile: 128 rows x 128 B
 constexpr uint32_t kSmemV = 16384;            // V^T: two 64-key halves of 64 rows x 128 B
 constexpr uint32_t kSmemStage0 = 32768;

@@ -256,6 +256,17 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
+// True in exactly one lane of a converged warp (the same lane every time).
+// Single-thread instructions (MMA, commit, bulk copies) issued under it keep
+// the rest of the warp's address arithmetic warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(p));
+  return p != 0;
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
