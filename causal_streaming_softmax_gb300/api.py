@@ -38,6 +38,13 @@ class AttnShape(ctypes.Structure):
                 ("head_begin", ctypes.c_int32), ("head_count", ctypes.c_int32)]
 
 
+class AttnDeviceBuffers(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("vt", ctypes.c_void_p),
+                ("dout", ctypes.c_void_p), ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("delta", ctypes.c_void_p), ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t),
+                ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dvt", ctypes.c_void_p)]
+
+
 class AttnError(RuntimeError):
     def __init__(self, fn, code):
         self.code = code
@@ -77,6 +84,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attn_version.restype = ctypes.c_int
     lib.attn_last_cuda_error.restype = ctypes.c_char_p
     lib.attn_selftest_arith.argtypes = [vp, vp, vp, ctypes.c_int, vp]
+    lib.attn_step_host.argtypes = [ctypes.POINTER(AttnShape), ctypes.POINTER(AttnDeviceBuffers)] + \
+        [vp] * 10
+    lib.attn_step_host.restype = ctypes.c_int
     lib.attn_selftest_arith.restype = ctypes.c_int
     for name in ("attn_fwd", "attn_row_terms", "attn_bwd_keys", "attn_bwd_queries",
                  "attn_last_device_error", "attn_selftest_wait_timeout"):
@@ -301,17 +311,22 @@ class DeviceInputs:
         self.dout = torch.empty((B, H, T, 64), dtype=torch.float16, device=dev)
 
 
-def forward_backward_host(s: Shape, host: HostProblem, dev_in: DeviceInputs, bufs: Buffers,
-                          stream=None) -> None:
-    """Host-to-host pass on one stream: copy the inputs in, run the four
-    calls, copy O, L, dQ, dK and dV^T back (asynchronous; synchronise the
-    stream before reading ``host``'s outputs)."""
-    st = stream if stream is not None else torch.cuda.current_stream()
-    with torch.cuda.stream(st):
-        for dst, src in ((dev_in.q, host.q), (dev_in.k, host.k), (dev_in.vt, host.vt),
-                         (dev_in.dout, host.dout)):
-            dst.copy_(src, non_blocking=True)
-        forward_backward(s, dev_in.q, dev_in.k, dev_in.vt, dev_in.dout, bufs, st)
-        for dst, src in ((host.o, bufs.o), (host.lse, bufs.lse), (host.dq, bufs.dq),
-                         (host.dk, bufs.dk), (host.dvt, bufs.dvt)):
-            dst.copy_(src, non_blocking=True)
+def attn_step_host(s: Shape, host: HostProblem, dev_in: DeviceInputs, bufs: Buffers,
+                   stream=None) -> None:
+    """Host-to-host pass through the C ABI: copies the inputs in, runs the
+    four calls and copies O, L, dQ, dK and dV^T back, the copies overlapped
+    with the kernels (asynchronous; synchronise the stream before reading
+    ``host``'s outputs)."""
+    dev = AttnDeviceBuffers(dev_in.q.data_ptr(), dev_in.k.data_ptr(), dev_in.vt.data_ptr(),
+                            dev_in.dout.data_ptr(), bufs.o.data_ptr(), bufs.lse.data_ptr(),
+                            bufs.delta.data_ptr(), bufs.ws.data_ptr(),
+                            bufs.ws.numel() * bufs.ws.element_size(), bufs.dq.data_ptr(),
+                            bufs.dk.data_ptr(), bufs.dvt.data_ptr())
+    shape = s.c_struct()
+    _check("attn_step_host", load_library().attn_step_host(
+        ctypes.byref(shape), ctypes.byref(dev), host.q.data_ptr(), host.k.data_ptr(),
+        host.vt.data_ptr(), host.dout.data_ptr(), host.o.data_ptr(), host.lse.data_ptr(),
+        host.dq.data_ptr(), host.dk.data_ptr(), host.dvt.data_ptr(), _stream_ptr(stream)))
+
+
+forward_backward_host = attn_step_host

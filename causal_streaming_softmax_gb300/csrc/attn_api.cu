@@ -109,6 +109,8 @@ int validate_shape(const attn_shape* s, Dims* d) {
   d->kv_count = count;
   d->nt = (s->seq + kTile - 1) / kTile;
   d->npairs = s->causal ? (long long)d->nt * (d->nt + 1) / 2 : (long long)d->nt * d->nt;
+  d->ws_heads = 0;
+  d->ws_h0 = 0;
   return ATTN_OK;
 }
 

@@ -26,6 +26,8 @@ struct Dims {
   int kv_count;
   int nt;               // ceil(T / 128)
   long long npairs;     // workspace tiles per query head
+  int ws_heads;         // query heads per batch in the workspace layout (0: kv_count * G)
+  int ws_h0;            // layout index of the chunk's first query head
   // workspace tile index of (query tile i, key tile j)
   __host__ __device__ long long pair(int i, int j) const {
     return causal ? (long long)i * (i + 1) / 2 + j : (long long)i * nt + j;

@@ -250,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 13) {
     // ---------------- store: dS^T of each step into the workspace ----------------
     if (lane == 0 && n_steps > 0) {
-      const int Hc = d.kv_count * d.G;
-      const int h_local0 = (kv - d.kv_begin) * d.G;
+      const int Hc = d.ws_heads ? d.ws_heads : d.kv_count * d.G;
+      const int h_local0 = d.ws_h0 + (kv - d.kv_begin) * d.G;
       int g = 0, rem = 0;
       for (int n = 0; n < n_steps; ++n) {
         // every row of the step's dS^T is in shared memory (and fenced for

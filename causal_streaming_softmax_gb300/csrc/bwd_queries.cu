@@ -81,8 +81,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int q0 = it * kBM;
   int n_kt = 0;
   if (q0 < len) n_kt = d.causal ? it + 1 : (len + kBN - 1) / kBN;
-  const int Hc = d.kv_count * d.G;
-  const long long tile0 = ((long long)b * Hc + h_local) * d.npairs;
+  const int Hc = d.ws_heads ? d.ws_heads : d.kv_count * d.G;
+  const long long tile0 = ((long long)b * Hc + d.ws_h0 + h_local) * d.npairs;
 
   WaitCtl wc{a.err, a.wait_ns, &s_abort};
 

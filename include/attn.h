@@ -156,6 +156,53 @@ ATTN_API int attn_bwd_queries(const attn_shape* shape, const uint16_t* k,
                      void* stream);
 
 /*
+ * Device buffers of one whole problem, as attn_step_host uses them.  All
+ * device pointers, 16-byte aligned, laid out as the calls above state:
+ * q, dout [B][H][T][64] and k [B][Hkv][T][64], vt [B][Hkv][64][T] (binary16);
+ * o [B][T][H*64] (binary16); lse, delta [B][H][T]; dq [B][H][T][64],
+ * dk [B][Hkv][T][64], dvt [B][Hkv][64][T] (binary32); ws the dS workspace of
+ * ws_bytes >= attn_bwd_workspace_bytes.  Owned by the caller.
+ */
+typedef struct attn_device_buffers {
+  uint16_t* q;
+  uint16_t* k;
+  uint16_t* vt;
+  uint16_t* dout;
+  uint16_t* o;
+  float* lse;
+  float* delta;
+  void* ws;
+  size_t ws_bytes;
+  float* dq;
+  float* dk;
+  float* dvt;
+} attn_device_buffers;
+
+/*
+ * attn_step_host - one whole forward and backward from host memory to host
+ * memory: copies h_q, h_k, h_vt, h_dout into the device buffers, runs
+ * attn_fwd, attn_row_terms, attn_bwd_keys and attn_bwd_queries, and copies
+ * O, L, dQ, dK and dV^T back into h_o, h_lse, h_dq, h_dk, h_dvt (layouts as
+ * in attn_device_buffers).  The method's pages have no host-transfer step;
+ * this is the library's runtime around the path.  The copies overlap the
+ * kernels: dO goes in while the forward runs, O and L come out during the
+ * backward, dK and dV^T during the dQ pass, and dQ in two halves, the first
+ * while the second is computed; a second stream owned by the library (one
+ * per device) carries them, and `stream` waits for it before the call's work
+ * ends.  Asynchronous: returns once everything is enqueued; the host outputs
+ * are valid after `stream` completes, and no host buffer may be touched
+ * before then.  Host buffers should be page-locked (pageable memory works,
+ * but its copies do not overlap).  The shape must cover every K/V head
+ * (head_begin = 0, head_count = 0 or Hkv); seq_lens, if any, is a device
+ * array.  Errors as the calls above; a CUDA failure while enqueueing
+ * returns ATTN_ERR_CUDA with the work enqueued so far left on the streams.
+ */
+ATTN_API int attn_step_host(const attn_shape* shape, const attn_device_buffers* dev,
+                            const uint16_t* h_q, const uint16_t* h_k, const uint16_t* h_vt,
+                            const uint16_t* h_dout, uint16_t* h_o, float* h_lse, float* h_dq,
+                            float* h_dk, float* h_dvt, void* stream);
+
+/*
  * attn_bwd_noalloc - the key pass and the dQ pass (what attn_bwd_keys and
  * then attn_bwd_queries compute) without a caller-supplied workspace.  The
  * method's pages have no counterpart to this entry point.  It is for callers

@@ -114,3 +114,27 @@ def test_python_binding_checks_types():
     cpu = torch.zeros(1, 2, 128, 64, dtype=torch.float16)
     with pytest.raises(ValueError):
         api.attn_fwd(s, cpu, cpu, cpu, cpu, cpu)
+
+
+def test_step_host_rejections(lib):
+    """attn_step_host refuses a head chunk, missing buffers and misaligned or
+    short device buffers before anything is enqueued."""
+    p = 0x1000
+    h = [p] * 8  # h_q .. h_dk; h_dvt and the stream follow
+    dev = api.AttnDeviceBuffers(p, p, p, p, p, p, p, p, 1 << 40, p, p, p)
+    chunk = shape(head_begin=0, head_count=1)
+    assert lib.attn_step_host(ctypes.byref(chunk), ctypes.byref(dev), *h, p, None) == \
+        api.ATTN_ERR_SHAPE
+    s = shape()
+    assert lib.attn_step_host(ctypes.byref(s), None, *h, p, None) == api.ATTN_ERR_NULL
+    assert lib.attn_step_host(ctypes.byref(s), ctypes.byref(dev), *h, None, None) == \
+        api.ATTN_ERR_NULL
+    no_ws = api.AttnDeviceBuffers(p, p, p, p, p, p, p, None, 1 << 40, p, p, p)
+    assert lib.attn_step_host(ctypes.byref(s), ctypes.byref(no_ws), *h, p, None) == \
+        api.ATTN_ERR_NULL
+    bad = api.AttnDeviceBuffers(p, p, p, p, p, p, p, p + 8, 1 << 40, p, p, p)
+    assert lib.attn_step_host(ctypes.byref(s), ctypes.byref(bad), *h, p, None) == \
+        api.ATTN_ERR_ALIGN
+    short = api.AttnDeviceBuffers(p, p, p, p, p, p, p, p, 16, p, p, p)
+    assert lib.attn_step_host(ctypes.byref(s), ctypes.byref(short), *h, p, None) == \
+        api.ATTN_ERR_WORKSPACE

@@ -202,3 +202,33 @@ def test_workload_sampled(cuda_device, cfg):
         heads = [0, G - 1, H - 1]
         kv_heads = [w.kv_heads - 1]
     _check_sampled(w, inp, gpu, heads, kv_heads, batches, rng)
+
+
+@pytest.mark.parametrize("B,T,H,Hkv,causal,lens", [
+    (1, 512, 8, 2, True, None),
+    (3, 384, 4, 2, False, [100, 384, 257]),   # batches: the split dQ copy is strided
+    (2, 256, 2, 1, True, None),               # one K/V head: dQ in one piece
+])
+def test_step_host_matches_device_path(cuda_device, B, T, H, Hkv, causal, lens):
+    """attn_step_host (host buffers in and out, copies overlapped with the
+    kernels) gives the same bits as the four device calls."""
+    import torch
+    from causal_streaming_softmax_gb300 import api
+    inp = workloads.make_custom_inputs(B, T, H, Hkv, causal=causal, lens=lens, seed=T + B)
+    ref = run_gpu(inp, causal=causal)
+    ln = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
+    s = api.Shape(B, T, H, Hkv, causal=causal, seq_lens=ln)
+    host = api.HostProblem(s, *(torch.from_numpy(inp[n]) for n in ("q", "k", "vt", "dout")))
+    dev_in = api.DeviceInputs(s)
+    bufs = api.Buffers(s)
+    for out in (host.o, host.lse, host.dq, host.dk, host.dvt):
+        out.fill_(float("nan"))
+    stream = torch.cuda.Stream()
+    for _ in range(2):
+        api.attn_step_host(s, host, dev_in, bufs, stream)
+        stream.synchronize()
+        assert api.last_device_error() == 0
+        got = dict(o=host.o.numpy(), lse=host.lse.numpy(), dq=host.dq.numpy(),
+                   dk=host.dk.numpy(), dvt=host.dvt.numpy())
+        for name, val in got.items():
+            assert np.array_equal(val, ref[name], equal_nan=True), name
