@@ -75,6 +75,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attn_bwd_workspace_bytes.restype = sz
     lib.attn_bwd_keys.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     lib.attn_bwd_queries.argtypes = [sp, vp, vp, sz, vp, vp]
+    lib.attn_bwd_queries_fused.argtypes = [sp] + [vp] * 8
+    lib.attn_bwd_queries_fused.restype = ctypes.c_int
     lib.attn_error_string.argtypes = [ctypes.c_int]
     lib.attn_error_string.restype = ctypes.c_char_p
     lib.attn_last_device_error.argtypes = [vp]
@@ -195,17 +197,18 @@ def _chunk_heads(s: Shape):
 
 
 def attn_bwd_keys(s: Shape, q, k, vt, dout, lse, delta, ws, dk, dvt, stream=None) -> None:
+    """``ws=None`` runs the key pass without storing dS (for attn_bwd_queries_fused)."""
     B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
-    if not (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.dtype == torch.uint8
-            and ws.is_contiguous()):
-        raise TypeError("ws must be a contiguous uint8 CUDA tensor")
+    if ws is not None and not (isinstance(ws, torch.Tensor) and ws.is_cuda
+                               and ws.dtype == torch.uint8 and ws.is_contiguous()):
+        raise TypeError("ws must be a contiguous uint8 CUDA tensor or None")
     args = (_want(q, "q", torch.float16, (B, H, T, 64)),
             _want(k, "k", torch.float16, (B, Hkv, T, 64)),
             _want(vt, "vt", torch.float16, (B, Hkv, 64, T)),
             _want(dout, "dout", torch.float16, (B, H, T, 64)),
             _want(lse, "lse", torch.float32, (B, H, T)),
             _want(delta, "delta", torch.float32, (B, H, T)),
-            ws.data_ptr(), ws.numel(),
+            None if ws is None else ws.data_ptr(), 0 if ws is None else ws.numel(),
             _want(dk, "dk", torch.float32, (B, Hkv, T, 64)),
             _want(dvt, "dvt", torch.float32, (B, Hkv, 64, T)))
     shape = s.c_struct()
@@ -223,6 +226,20 @@ def attn_bwd_queries(s: Shape, k, ws, dq, stream=None) -> None:
     shape = s.c_struct()
     _check("attn_bwd_queries",
            load_library().attn_bwd_queries(ctypes.byref(shape), *args, _stream_ptr(stream)))
+
+
+def attn_bwd_queries_fused(s: Shape, q, k, vt, dout, lse, delta, dq, stream=None) -> None:
+    B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
+    args = (_want(q, "q", torch.float16, (B, H, T, 64)),
+            _want(k, "k", torch.float16, (B, Hkv, T, 64)),
+            _want(vt, "vt", torch.float16, (B, Hkv, 64, T)),
+            _want(dout, "dout", torch.float16, (B, H, T, 64)),
+            _want(lse, "lse", torch.float32, (B, H, T)),
+            _want(delta, "delta", torch.float32, (B, H, T)),
+            _want(dq, "dq", torch.float32, (B, H, T, 64)))
+    shape = s.c_struct()
+    _check("attn_bwd_queries_fused", load_library().attn_bwd_queries_fused(
+        ctypes.byref(shape), *args, _stream_ptr(stream)))
 
 
 def last_device_error(stream=None) -> int:
@@ -255,9 +272,10 @@ def selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None) -> int:
 
 
 class Buffers:
-    """Device buffers of one forward + backward problem (boundary layouts)."""
+    """Device buffers of one forward + backward problem (boundary layouts);
+    ``workspace=False`` leaves out the dS workspace (for the fused dQ pass)."""
 
-    def __init__(self, s: Shape, device=None):
+    def __init__(self, s: Shape, device=None, workspace: bool = True):
         dev = device or torch.device("cuda")
         B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
         self.o = torch.empty((B, T, H * 64), dtype=torch.float16, device=dev)
@@ -266,15 +284,23 @@ class Buffers:
         self.dq = torch.empty((B, H, T, 64), dtype=torch.float32, device=dev)
         self.dk = torch.empty((B, Hkv, T, 64), dtype=torch.float32, device=dev)
         self.dvt = torch.empty((B, Hkv, 64, T), dtype=torch.float32, device=dev)
-        self.ws = alloc_workspace(s, dev)
+        self.ws = alloc_workspace(s, dev) if workspace else None
 
 
-def forward_backward(s: Shape, q, k, vt, dout, bufs: Buffers, stream=None) -> Buffers:
-    """One pass of the whole path: attn_fwd, attn_row_terms, attn_bwd_keys, attn_bwd_queries."""
+def forward_backward(s: Shape, q, k, vt, dout, bufs: Buffers, stream=None,
+                     fused_dq: bool = False) -> Buffers:
+    """One pass of the whole path: attn_fwd, attn_row_terms, attn_bwd_keys,
+    attn_bwd_queries; with ``fused_dq`` the key pass stores no dS and
+    attn_bwd_queries_fused recomputes it (``bufs.ws`` unused)."""
     attn_fwd(s, q, k, vt, bufs.o, bufs.lse, stream)
     attn_row_terms(s, bufs.o, dout, bufs.delta, stream)
-    attn_bwd_keys(s, q, k, vt, dout, bufs.lse, bufs.delta, bufs.ws, bufs.dk, bufs.dvt, stream)
-    attn_bwd_queries(s, k, bufs.ws, bufs.dq, stream)
+    if fused_dq:
+        attn_bwd_keys(s, q, k, vt, dout, bufs.lse, bufs.delta, None, bufs.dk, bufs.dvt, stream)
+        attn_bwd_queries_fused(s, q, k, vt, dout, bufs.lse, bufs.delta, bufs.dq, stream)
+    else:
+        attn_bwd_keys(s, q, k, vt, dout, bufs.lse, bufs.delta, bufs.ws, bufs.dk, bufs.dvt,
+                      stream)
+        attn_bwd_queries(s, k, bufs.ws, bufs.dq, stream)
     return bufs
 
 

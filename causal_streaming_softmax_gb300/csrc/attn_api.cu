@@ -211,15 +211,34 @@ int attn_bwd_keys(const attn_shape* shape, const uint16_t* q, const uint16_t* k,
   Dims d;
   int rc = validate_shape(shape, &d);
   if (rc != ATTN_OK) return rc;
-  if (!q || !k || !vt || !dout || !lse || !delta || !ds_ws || !dk || !dvt) return ATTN_ERR_NULL;
+  // no workspace at all (null, 0 bytes): dS is not stored
+  const bool store = !(ds_ws == nullptr && ws_bytes == 0);
+  if (!q || !k || !vt || !dout || !lse || !delta || (store && !ds_ws) || !dk || !dvt)
+    return ATTN_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(dout) || !aligned16(lse) ||
       !aligned16(delta) || !aligned16(ds_ws) || !aligned16(dk) || !aligned16(dvt))
     return ATTN_ERR_ALIGN;
-  if (ws_bytes < workspace_bytes_for(d)) return ATTN_ERR_WORKSPACE;
+  if (store && ws_bytes < workspace_bytes_for(d)) return ATTN_ERR_WORKSPACE;
   DevCtx ctx;
   if ((rc = device_context(&ctx)) != ATTN_OK) return rc;
   return launch_bwd_keys(d, ctx, q, k, vt, dout, lse, delta, static_cast<uint8_t*>(ds_ws), dk,
                          dvt, static_cast<cudaStream_t>(stream));
+}
+
+int attn_bwd_queries_fused(const attn_shape* shape, const uint16_t* q, const uint16_t* k,
+                           const uint16_t* vt, const uint16_t* dout, const float* lse,
+                           const float* delta, float* dq, void* stream) {
+  Dims d;
+  int rc = validate_shape(shape, &d);
+  if (rc != ATTN_OK) return rc;
+  if (!q || !k || !vt || !dout || !lse || !delta || !dq) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(delta) || !aligned16(dq))
+    return ATTN_ERR_ALIGN;
+  DevCtx ctx;
+  if ((rc = device_context(&ctx)) != ATTN_OK) return rc;
+  return launch_bwd_fused_q(d, ctx, q, k, vt, dout, lse, delta, dq,
+                            static_cast<cudaStream_t>(stream));
 }
 
 int attn_bwd_queries(const attn_shape* shape, const uint16_t* k, const void* ds_ws,

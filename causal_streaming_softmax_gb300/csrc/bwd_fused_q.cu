@@ -1,0 +1,381 @@
+// bwd_fused_q.cu - the fused query pass: dQ for one 128-query tile of one
+// query head per CTA, with S, P, dP and dS recomputed from Q, K, V, dO, L and
+// D instead of read back from a stored dS.
+//
+// Method (StreamingAttentionSM86.alpha, the query-side backward: the page-2
+// pass that forms S, P and dP again for a query tile and accumulates
+// dQ = s * sum_j dS_j K_j over the visible key tiles):
+//   S = Q K^T, P = 2^(S c - L), dP = dO V^T, dS = P (dP - D), dQ += dS K,
+// dS rounded to binary16 before its product, as in the key pass.  It trades
+// two recomputed products per tile pair for the dS workspace, whose size and
+// traffic grow as T^2: the key pass then runs without storing dS.
+//
+// GB300 design.
+//   warps 0-7   score gradients, thread = query row (tensor-memory lane);
+//               warps 0-3 take keys 0-63 of a key tile, warps 4-7 keys 64-127,
+//               each in two chunks of 32
+//   warp 8      TMA producer: Q and dO once, then per key tile K and V^T
+//               through a 4-stage ring
+//   warps 9-11  MMA issuers: S = Q K^T, dP = dO V^T (A = Q / dO copied into
+//               tensor memory once, B = the K tile K-major / the V^T tile as
+//               an MN-major V), dQ += dS K (A = dS from tensor memory, B = the
+//               K tile MN-major)
+// A query row's L and D are per-thread scalars.  The S and dP buffer is
+// released once the score-gradient warps hold its last chunk in registers,
+// so the next tile's products run during their arithmetic; dS goes into one
+// of two pair buffers, which gives dQ += dS K a tile to finish.
+//
+// Tensor memory (512 columns): Q 0-31, dO 32-63 (binary16 pairs); S 64-191,
+// dP 192-319; dS pair buffer b at 320+64b (keys 0-63 in its first 32
+// columns, 64-127 in the next 32); dQ 448-511.
+#include <math.h>
+
+#include <mutex>
+
+#include "attn_internal.h"
+#include "sm103.cuh"
+
+namespace css {
+namespace {
+
+constexpr int kBM = 128;  // queries per CTA
+constexpr int kBN = 128;  // keys per tile
+constexpr int kThreads = 384;
+constexpr int kStages = 4;
+constexpr uint32_t kSmemQ = 0, kSmemDO = 16384;
+constexpr uint32_t kSmemStage0 = 32768;
+constexpr uint32_t kStK = 0, kStVT = 16384;  // V^T: two 64-key halves of 64 rows x 128 B
+constexpr uint32_t kStageBytes = 32768;
+constexpr uint32_t kSmemBar = kSmemStage0 + kStages * kStageBytes;
+constexpr uint32_t kSmemBytes = kSmemBar + 256 + 1024;
+
+constexpr uint32_t kColQ = 0, kColDO = 32, kColS = 64, kColDP = 192, kColDS = 320, kColDQ = 448;
+constexpr uint32_t kTmemCols = 512;
+
+constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);   // Q (tmem) x K (K-major)
+constexpr uint32_t kIdescDP = idesc_f16_f32(128, 128, 0, 1);  // dO (tmem) x V (MN-major, from V^T)
+constexpr uint32_t kIdescDQ = idesc_f16_f32(128, 64, 0, 1);   // dS (tmem) x K (MN-major)
+
+enum {
+  BAR_QD_FULL = 0,                      // Q and dO tiles landed
+  BAR_QD_TMEM,                          // Q and dO in tensor memory (256 threads)
+  BAR_KV_FULL,                          // [stage] K and V^T landed
+  BAR_KV_EMPTY = BAR_KV_FULL + kStages, // [stage] dQ += dS K of the tile done
+  BAR_S_FULL = BAR_KV_EMPTY + kStages,  // S and dP of the tile done (2 commits)
+  BAR_LOADED,                           // S and dP are in registers (256 threads)
+  BAR_P_READY,                          // [2] dS of pair buffer b written (256 threads)
+  BAR_PK_FREE = BAR_P_READY + 2,        // [2] dQ += dS K has read pair buffer b
+  BAR_DONE = BAR_PK_FREE + 2,           // dQ complete
+  BAR_COUNT
+};
+static_assert(BAR_COUNT * 8 <= 256, "barrier area");
+
+struct FusedArgs {
+  Dims d;
+  const float* lse;
+  const float* delta;
+  float* dq;
+  uint32_t* err;
+  uint64_t wait_ns;
+};
+
+__device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
+
+static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+// dS = P (dP - D) with P = 2^(S c - L) for 32 keys of one query row, packed
+// to binary16 pairs.  MASK zeroes the keys outside [0, lim) (local indices).
+template <bool MASK>
+__device__ __forceinline__ void score_gradients(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
+                                                float c, float L, float D, int lim,
+                                                uint32_t (&dd)[16]) {
+  const float2 c2 = make_float2(c, c), nl = make_float2(-L, -L), nd = make_float2(-D, -D);
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const float2 t = __ffma2_rn(make_float2(as_f(sv[e]), as_f(sv[e + 1])), c2, nl);
+    float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    if (MASK) {
+      if (e >= lim) p.x = 0.f;
+      if (e + 1 >= lim) p.y = 0.f;
+    }
+    const float2 g = __fadd2_rn(make_float2(as_f(dv[e]), as_f(dv[e + 1])), nd);
+    const float2 ds = __fmul2_rn(p, g);
+    dd[e >> 1] = pack_f16x2(ds.x, ds.y);
+  }
+}
+
+// 12 warps on four schedulers allow 168 registers a thread.
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_fused_q_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_vt,
+                       const __grid_constant__ CUtensorMap tm_do, const FusedArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const sgen = smem_raw + (sbase - smem_u32(smem_raw));
+  const uint32_t bar0 = sbase + kSmemBar;
+#define BAR(i) (bar0 + 8u * (uint32_t)(i))
+
+  const Dims& d = a.d;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = d.kv_begin * d.G + blockIdx.x;
+  const int kv = h / d.G;
+  const int it = (int)gridDim.y - 1 - (int)blockIdx.y;  // heaviest causal tiles first
+  const int b = blockIdx.z;
+  const int T = d.T;
+  int len = T;
+  if (d.lens) {
+    len = d.lens[b];
+    len = len < 0 ? 0 : (len > T ? T : len);
+  }
+  const int q0 = it * kBM;
+  int n_kt = 0;
+  if (q0 < len) n_kt = d.causal ? it + 1 : (len + kBN - 1) / kBN;
+  if (d.causal && n_kt * kBN > len) n_kt = (len + kBN - 1) / kBN;
+
+  WaitCtl wc{a.err, a.wait_ns, &s_abort};
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    mbar_init(BAR(BAR_QD_FULL), 1);
+    mbar_init(BAR(BAR_QD_TMEM), 256);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(BAR(BAR_KV_FULL + s), 1);
+      mbar_init(BAR(BAR_KV_EMPTY + s), 1);
+    }
+    mbar_init(BAR(BAR_S_FULL), 2);
+    mbar_init(BAR(BAR_LOADED), 256);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(BAR(BAR_P_READY + u), 256);
+      mbar_init(BAR(BAR_PK_FREE + u), 1);
+    }
+    mbar_init(BAR(BAR_DONE), 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 9) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 8) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0 && n_kt > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_vt);
+      tma_prefetch_desc(&tm_do);
+      const int qplane = b * d.H + h;
+      const int kvplane = b * d.Hkv + kv;
+      mbar_arrive_expect_tx(BAR(BAR_QD_FULL), 32768);
+      tma_load_3d(sbase + kSmemQ, &tm_q, BAR(BAR_QD_FULL), 0, q0, qplane);
+      tma_load_3d(sbase + kSmemDO, &tm_do, BAR(BAR_QD_FULL), 0, q0, qplane);
+      int issued = 0;
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages && !mbar_wait(BAR(BAR_KV_EMPTY + s), ((j / kStages) - 1) & 1, wc)) break;
+        const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
+        mbar_arrive_expect_tx(BAR(BAR_KV_FULL + s), kStageBytes);
+        tma_load_3d(st + kStK, &tm_k, BAR(BAR_KV_FULL + s), 0, j * kBN, kvplane);
+        tma_load_3d(st + kStVT, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN, 0, kvplane);
+        tma_load_3d(st + kStVT + 8192, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN + 64, 0, kvplane);
+        issued = j + 1;
+      }
+      drain_wait(BAR(BAR_QD_FULL), 0, a.wait_ns);
+      for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
+        drain_wait(BAR(BAR_KV_FULL + j % kStages), (j / kStages) & 1, a.wait_ns);
+    }
+  } else if (warp >= 9) {
+    // ---------------- MMA issuers ----------------
+    const int role = warp - 9;  // 0: S = Q K^T, 1: dP = dO V^T, 2: dQ += dS K
+    if (lane == 0 && n_kt > 0) {
+      bool ok = true;
+      if (role < 2) {
+        ok = mbar_wait(BAR(BAR_QD_TMEM), 0, wc);
+        const uint32_t a_col = role == 0 ? kColQ : kColDO;
+        const uint32_t dcol = tmem + (role == 0 ? kColS : kColDP);
+        for (int j = 0; ok && j < n_kt; ++j) {
+          const int s = j % kStages;
+          if (!mbar_wait(BAR(BAR_KV_FULL + s), (j / kStages) & 1, wc)) break;
+          // the score-gradient warps hold tile j-1's S and dP in registers
+          if (j >= 1 && !mbar_wait(BAR(BAR_LOADED), (j - 1) & 1, wc)) break;
+          tc_fence_after();
+          const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
+          // reduction over d: four K=16 steps.  K: 32 B along its K-major
+          // rows; V from V^T: 16 rows of d (2 KiB) a step, its two 64-key
+          // halves 8 KiB apart
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bdesc = role == 0
+                                       ? sdesc_sw128(st + kStK + kk * 32, 16, 1024)
+                                       : sdesc_sw128(st + kStVT + kk * 2048, 8192, 1024);
+            mma_ts(dcol, tmem + a_col + kk * 8, bdesc, role == 0 ? kIdescS : kIdescDP, kk > 0);
+          }
+          mma_commit(BAR(BAR_S_FULL));
+        }
+      } else {
+        for (int j = 0; ok && j < n_kt; ++j) {
+          const int s = j % kStages;
+          const int pb = j & 1;
+          if (!mbar_wait(BAR(BAR_P_READY + pb), (j >> 1) & 1, wc)) break;
+          tc_fence_after();
+          const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
+          // reduction over the tile's 128 keys: 16 K rows (2 KiB) a step
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + kColDQ, tmem + kColDS + 64 * pb + 8 * kk,
+                   sdesc_sw128(st + kStK + kk * 2048, 8192, 1024), kIdescDQ,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(BAR(BAR_PK_FREE + pb));
+          mma_commit(BAR(BAR_KV_EMPTY + s));
+        }
+        mma_commit(BAR(BAR_DONE));
+      }
+    }
+  } else {
+    // ---------------- score gradients: thread = query row ----------------
+    const int wg = warp >> 2;  // keys 64wg..64wg+63 of each tile
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int q = q0 + r;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const float c = d.c;
+    const bool row_ok = q < len;
+    // keys below `lim` are valid for this row
+    int lim = row_ok ? len : 0;
+    if (d.causal) lim = min(lim, q + 1);
+    const size_t lrow = ((size_t)b * d.H + h) * T + q;
+    float L = 0.f, D = 0.f;
+    if (row_ok) {
+      L = a.lse[lrow];
+      D = a.delta[lrow];
+    }
+    bool ok = true;
+    if (n_kt > 0) {
+      // Q (warps 0-3) or dO (warps 4-7) row r into tensor memory as A operands
+      ok = mbar_wait_warp(BAR(BAR_QD_FULL), 0, wc);
+      uint32_t w[32];
+      const uint8_t* src = sgen + (wg == 0 ? kSmemQ : kSmemDO);
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + sw128_offset(r, ch));
+        w[4 * ch] = v.x, w[4 * ch + 1] = v.y, w[4 * ch + 2] = v.z, w[4 * ch + 3] = v.w;
+      }
+      tmem_st32(tmem + lane_base + (wg == 0 ? kColQ : kColDO), w);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(BAR(BAR_QD_TMEM));
+    }
+    for (int j = 0; ok && j < n_kt; ++j) {
+      const int pb = j & 1;
+      const int k0 = j * kBN + 64 * wg;  // this thread's first key
+      if (!mbar_wait_warp(BAR(BAR_S_FULL), j & 1, wc)) {
+        ok = false;
+        break;
+      }
+      // pair buffer pb was last read by dQ += dS K of tile j-2
+      if (j >= 2 && !mbar_wait_warp(BAR(BAR_PK_FREE + pb), ((j >> 1) - 1) & 1, wc)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t sv[32], dv[32];
+        const uint32_t col = 64 * wg + 32 * ch;
+        tmem_ld32x2_wait(tmem + lane_base + kColS + col, tmem + lane_base + kColDP + col, sv, dv);
+        if (ch == 1) {
+          // both chunks are in registers: the S and dP buffer is free
+          tc_fence_before();
+          mbar_arrive(BAR(BAR_LOADED));
+        }
+        const int kc = k0 + 32 * ch;
+        const int lim_local = lim - kc;
+        uint32_t dd[16];
+        if (lim_local < 32)
+          score_gradients<true>(sv, dv, c, L, D, lim_local, dd);
+        else
+          score_gradients<false>(sv, dv, c, L, D, lim_local, dd);
+        tmem_st16(tmem + lane_base + kColDS + 64 * pb + 32 * wg + 16 * ch, dd);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(BAR(BAR_P_READY + pb));
+    }
+
+    // ---------------- epilogue: dQ = s * sum; warp group w takes columns 32w.. ----------------
+    if (q < T) {
+      float* dst = a.dq + lrow * 64 + 32 * wg;
+      if (n_kt > 0) {
+        ok = mbar_wait_warp(BAR(BAR_DONE), 0, wc) && ok;
+        tc_fence_after();
+        uint32_t r0[32];
+        tmem_ld32_wait(tmem + lane_base + kColDQ + 32 * wg, r0);
+        float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          d4[u] = make_float4(as_f(r0[4 * u]) * d.scale, as_f(r0[4 * u + 1]) * d.scale,
+                              as_f(r0[4 * u + 2]) * d.scale, as_f(r0[4 * u + 3]) * d.scale);
+      } else {
+        float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) d4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    } else if (n_kt > 0) {
+      // rows past T still take part in the warp-wide tensor-memory load
+      ok = mbar_wait_warp(BAR(BAR_DONE), 0, wc) && ok;
+      tc_fence_after();
+      uint32_t r0[32];
+      tmem_ld32_wait(tmem + lane_base + kColDQ + 32 * wg, r0);
+    }
+    (void)ok;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    if (n_kt > 0) drain_wait(BAR(BAR_DONE), 0, a.wait_ns);
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+#undef BAR
+}
+
+}  // namespace
+
+int launch_bwd_fused_q(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16_t* k,
+                       const uint16_t* vt, const uint16_t* dout, const float* lse,
+                       const float* delta, float* dq, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, tdo;
+  const uint64_t T = (uint64_t)d.T;
+  if (!encode_tmap_3d(&tq, q, 64, T, (uint64_t)d.B * d.H, 128, T * 128, 64, kBM) ||
+      !encode_tmap_3d(&tdo, dout, 64, T, (uint64_t)d.B * d.H, 128, T * 128, 64, kBM) ||
+      !encode_tmap_3d(&tk, k, 64, T, (uint64_t)d.B * d.Hkv, 128, T * 128, 64, kBN) ||
+      !encode_tmap_3d(&tv, vt, T, 64, (uint64_t)d.B * d.Hkv, T * 2, T * 128, 64, 64))
+    return ATTN_ERR_CUDA;
+  static std::once_flag attr_once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static cudaError_t attr_status[64];
+  std::call_once(attr_once[dev & 63], [dev] {
+    attr_status[dev & 63] = cudaFuncSetAttribute(
+        bwd_fused_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (attr_status[dev & 63] != cudaSuccess) return cuda_status(attr_status[dev & 63]);
+  FusedArgs args{d, lse, delta, dq, ctx.err, ctx.wait_ns};
+  dim3 grid(d.kv_count * d.G, d.nt, d.B);
+  bwd_fused_q_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, args);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace css

@@ -249,7 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 13) {
     // ---------------- store: dS^T of each step into the workspace ----------------
-    if (lane == 0 && n_steps > 0) {
+    // (no workspace: dS is not kept, for a dQ pass that recomputes it)
+    if (lane == 0 && n_steps > 0 && a.ws != nullptr) {
       const int Hc = d.ws_heads ? d.ws_heads : d.kv_count * d.G;
       const int h_local0 = d.ws_h0 + (kv - d.kv_begin) * d.G;
       int g = 0, rem = 0;
@@ -328,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = k0 + r;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float c = d.c;
+    const bool store_ds = a.ws != nullptr;
     bool ok = true;
     if (n_steps > 0) {
       // K (warps 0-3) or V (warps 4-7) row r into tensor memory as A operands
@@ -403,22 +405,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st16(tmem + lane_base + pk, pp);
       tmem_st16(tmem + lane_base + pk + 32, dd);
 
-      // shared dS^T buffer n % 3 was last filled at step n-3: its bulk store has read it
-      const int dsbuf = n % kDSBufs;
-      if (n >= kDSBufs &&
-          !mbar_wait_warp(BAR(BAR_DS_STORED + dsbuf), ((n / kDSBufs) - 1) & 1, wc)) {
-        ok = false;
-        break;
-      }
-      // dS^T row r, queries 32wg..32wg+31 of this 64-query half: chunks 4wg..4wg+3
-      const uint32_t dsb = sbase + kSmemDS0 + dsbuf * kDSHalf;
+      if (store_ds) {
+        // shared dS^T buffer n % 3 was last filled at step n-3: its bulk store has read it
+        const int dsbuf = n % kDSBufs;
+        if (n >= kDSBufs &&
+            !mbar_wait_warp(BAR(BAR_DS_STORED + dsbuf), ((n / kDSBufs) - 1) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        // dS^T row r, queries 32wg..32wg+31 of this 64-query half: chunks 4wg..4wg+3
+        const uint32_t dsb = sbase + kSmemDS0 + dsbuf * kDSHalf;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        st_shared_v4(dsb + sw128_offset(r, 4 * wg + u), dd[4 * u], dd[4 * u + 1], dd[4 * u + 2],
-                     dd[4 * u + 3]);
+        for (int u = 0; u < 4; ++u)
+          st_shared_v4(dsb + sw128_offset(r, 4 * wg + u), dd[4 * u], dd[4 * u + 1],
+                       dd[4 * u + 2], dd[4 * u + 3]);
+        fence_proxy_async_shared();
+      }
       tmem_st_wait();
       tc_fence_before();
-      fence_proxy_async_shared();
       mbar_arrive(BAR(BAR_P_READY + pb));
     }
 

@@ -17,6 +17,7 @@ namespace css {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kRowsPerBlock = kThreads / 8;  // T is a multiple of 64
 
 __device__ __forceinline__ float dot8(uint4 a, uint4 b) {
   const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
@@ -32,31 +33,24 @@ __device__ __forceinline__ float dot8(uint4 a, uint4 b) {
   return acc;
 }
 
+// Grid (T / 32, H, B): a block takes 32 consecutive rows of one (batch,
+// head), so no thread divides by a runtime size.
 __global__ void __launch_bounds__(kThreads)
     row_terms_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
-                     float* __restrict__ delta, int B, int T, int H,
-                     const int32_t* __restrict__ lens) {
-  const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
-  const long long row = gid >> 3;  // (b * H + h) * T + t
+                     float* __restrict__ delta, int T, int H, const int32_t* __restrict__ lens) {
+  const int t = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 3);
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
   const int part = threadIdx.x & 7;
-  const long long nrows = (long long)B * H * T;
-  const bool active = row < nrows;
-  float acc = 0.f;
-  int t = 0, b = 0;
-  if (active) {
-    t = (int)(row % T);
-    const long long bh = row / T;
-    const int h = (int)(bh % H);
-    b = (int)(bh / H);
-    const uint4 dv = __ldg(reinterpret_cast<const uint4*>(dout + row * 64) + part);
-    const uint4 ov = __ldg(
-        reinterpret_cast<const uint4*>(o + (((long long)b * T + t) * H + h) * 64) + part);
-    acc = dot8(dv, ov);
-  }
+  const size_t row = ((size_t)b * H + h) * T + t;  // [B][H][T]
+  const uint4 dv = __ldg(reinterpret_cast<const uint4*>(dout + row * 64) + part);
+  const uint4 ov =
+      __ldg(reinterpret_cast<const uint4*>(o + (((size_t)b * T + t) * H + h) * 64) + part);
+  float acc = dot8(dv, ov);
   acc += __shfl_xor_sync(0xffffffffu, acc, 1);
   acc += __shfl_xor_sync(0xffffffffu, acc, 2);
   acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-  if (active && part == 0) {
+  if (part == 0) {
     int len = T;
     if (lens) {
       len = lens[b];
@@ -103,11 +97,9 @@ int launch_arith_probe(const float* x, uint32_t* packed, float* e2, int n, cudaS
 int launch_row_terms(const Dims& d, const DevCtx& ctx, const uint16_t* o, const uint16_t* dout,
                      float* delta, cudaStream_t stream) {
   (void)ctx;
-  const long long threads = (long long)d.B * d.H * d.T * 8;
-  const long long blocks = (threads + kThreads - 1) / kThreads;
-  if (blocks > 0x7FFFFFFFll) return ATTN_ERR_SHAPE;
-  row_terms_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(o, dout, delta, d.B, d.T, d.H,
-                                                               d.lens);
+  if (d.H > 65535 || d.B > 65535) return ATTN_ERR_SHAPE;
+  dim3 grid(d.T / kRowsPerBlock, d.H, d.B);
+  row_terms_kernel<<<grid, kThreads, 0, stream>>>(o, dout, delta, d.T, d.H, d.lens);
   return cuda_status(cudaGetLastError());
 }
 

@@ -138,7 +138,9 @@ ATTN_API size_t attn_bwd_workspace_bytes(const attn_shape* shape);
  * dV += P^T dO and dK += dS^T Q over every query head of the group; dS^T is
  * stored (binary16) into ds_ws.  Writes dk = s * sum and dvt (unscaled) for
  * the chunk's K/V heads.  Needs lse from attn_fwd and delta from
- * attn_row_terms.  ds_ws: device, ws_bytes >= attn_bwd_workspace_bytes.
+ * attn_row_terms.  ds_ws: device, ws_bytes >= attn_bwd_workspace_bytes;
+ * or ds_ws = NULL with ws_bytes = 0, in which case dS is not stored (for
+ * callers that take dQ from attn_bwd_queries_fused instead).
  */
 ATTN_API int attn_bwd_keys(const attn_shape* shape, const uint16_t* q, const uint16_t* k,
                   const uint16_t* vt, const uint16_t* dout, const float* lse,
@@ -154,6 +156,24 @@ ATTN_API int attn_bwd_keys(const attn_shape* shape, const uint16_t* q, const uin
 ATTN_API int attn_bwd_queries(const attn_shape* shape, const uint16_t* k,
                      const void* ds_ws, size_t ws_bytes, float* dq,
                      void* stream);
+
+/*
+ * Fused query pass (the page-2 query-side backward of
+ * StreamingAttentionSM86.alpha, which forms S, P and dP again for a query
+ * tile): for each 128-query block, S = Q K^T, P = 2^(S c - L),
+ * dP = dO V^T and dS = P (dP - D) are recomputed for every visible key block
+ * and dQ = s * sum of dS K is accumulated; dS is rounded to binary16 before
+ * its product, as in the key pass.  Needs no workspace: pair it with
+ * attn_bwd_keys(..., NULL, 0, ...).  It recomputes two products per tile pair
+ * to avoid the dS workspace, whose size and traffic grow as T^2 (2 B per
+ * visible (query, key) pair and head).  Reads q, k, vt, dout, lse (from
+ * attn_fwd) and delta (from attn_row_terms); writes dq for the chunk's
+ * query heads.  Device pointers, 16-byte aligned, layouts as above.
+ */
+ATTN_API int attn_bwd_queries_fused(const attn_shape* shape, const uint16_t* q,
+                                    const uint16_t* k, const uint16_t* vt,
+                                    const uint16_t* dout, const float* lse,
+                                    const float* delta, float* dq, void* stream);
 
 /*
  * Device buffers of one whole problem, as attn_step_host uses them.  All

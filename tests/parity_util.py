@@ -13,7 +13,7 @@ L_TOL = 1e-4
 GRAD_TOL = 1e-2
 
 
-def run_gpu(inp, *, causal, scale=0.125, device="cuda"):
+def run_gpu(inp, *, causal, scale=0.125, device="cuda", fused_dq=False):
     import torch
     from causal_streaming_softmax_gb300 import api
     q = torch.from_numpy(inp["q"]).to(device)
@@ -25,8 +25,8 @@ def run_gpu(inp, *, causal, scale=0.125, device="cuda"):
     lens = None if inp.get("lens") is None else torch.from_numpy(
         np.ascontiguousarray(inp["lens"], dtype=np.int32)).to(device)
     s = api.Shape(B, T, H, Hkv, causal=causal, scale=scale, seq_lens=lens)
-    bufs = api.Buffers(s)
-    api.forward_backward(s, q, k, vt, dout, bufs)
+    bufs = api.Buffers(s, workspace=not fused_dq)
+    api.forward_backward(s, q, k, vt, dout, bufs, fused_dq=fused_dq)
     torch.cuda.synchronize()
     rc = api.last_device_error()
     assert rc == 0, "device error %d" % rc

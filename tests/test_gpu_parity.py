@@ -232,3 +232,55 @@ def test_step_host_matches_device_path(cuda_device, B, T, H, Hkv, causal, lens):
                    dk=host.dk.numpy(), dvt=host.dvt.numpy())
         for name, val in got.items():
             assert np.array_equal(val, ref[name], equal_nan=True), name
+
+
+# ---------------------------------------------------------------------------
+# the fused query pass: dQ with S, P, dP recomputed, the key pass storing no dS
+# ---------------------------------------------------------------------------
+FUSED = [
+    (1, 128, 2, 1, True, None),
+    (1, 64, 1, 1, True, None),
+    (1, 192, 4, 2, True, None),           # ragged tail: the last query tile is half empty
+    (2, 256, 4, 4, False, [1, 256]),
+    (4, 256, 2, 1, False, [63, 64, 65, 200]),
+    (3, 384, 4, 2, True, [1, 129, 384]),
+    (2, 1024, 2, 2, False, [600, 1000]),
+    (1, 1024, 8, 8, True, None),
+]
+
+
+@pytest.mark.parametrize("B,T,H,Hkv,causal,lens", FUSED)
+def test_fused_dq_against_oracle(cuda_device, B, T, H, Hkv, causal, lens):
+    inp = workloads.make_custom_inputs(B, T, H, Hkv, causal=causal, lens=lens, seed=T + 7 * H)
+    gpu = run_gpu(inp, causal=causal, fused_dq=True)
+    compare_full(gpu, _full(inp, causal), inp)
+
+
+def test_fused_dq_sharp_softmax(cuda_device):
+    inp = workloads.make_custom_inputs(1, 512, 8, 2, causal=True, q_std=4.0, seed=34)
+    gpu = run_gpu(inp, causal=True, fused_dq=True)
+    compare_full(gpu, _full(inp, True), inp)
+
+
+def test_key_pass_without_store_same_bits(cuda_device):
+    """The key pass that stores no dS gives the same dK and dV^T bits, and
+    the fused dQ is deterministic run to run."""
+    inp = workloads.make_custom_inputs(2, 512, 8, 2, causal=True, lens=[300, 512], seed=12)
+    stored = run_gpu(inp, causal=True)
+    fused = run_gpu(inp, causal=True, fused_dq=True)
+    again = run_gpu(inp, causal=True, fused_dq=True)
+    for name in ("o", "lse", "delta", "dk", "dvt"):
+        assert np.array_equal(stored[name], fused[name], equal_nan=True), name
+    assert np.array_equal(fused["dq"], again["dq"])
+    assert rel_fro(fused["dq"], stored["dq"]) <= 1e-3
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_fused_dq_workload_sampled(cuda_device, cfg):
+    w = workloads.WORKLOADS[cfg]
+    inp = workloads.make_inputs(w)
+    gpu = run_gpu(inp, causal=w.causal, scale=w.scale, fused_dq=True)
+    rng = np.random.default_rng(200 + cfg)
+    G = w.group
+    _check_sampled(w, inp, gpu, [0, G - 1, w.heads - 1], [w.kv_heads - 1], [0], rng)
