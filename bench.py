@@ -14,10 +14,13 @@ non-causal length-masked workload counts 4 d H sum(len^2).
 Reported in one JSON line (rank 0): ``value`` is device throughput with the
 inputs resident in HBM (L2 flushed before every timed step by a 256 MiB
 write, outside the timed events), ``e2e`` the same metric through the
-host-buffer API (pinned host -> device copies, the four calls, device ->
-host copies of O, L, dQ, dK, dV^T, all inside the timed region),
-``roofline`` the dominant kernel against the measured tensor peak, and
-``cpu_baseline`` the binary64 oracle on a bounded sample timed on the host.
+host-buffer C-ABI call attn_step_host (pinned host -> device copies, the
+four kernels, device -> host copies of O, L, dQ, dK, dV^T, all inside the
+timed region, the copies overlapped with the kernels),
+``roofline`` the dominant kernel against the measured tensor peak,
+``cpu_baseline`` the binary64 oracle on a bounded sample timed on the host,
+and ``fused_dq_variant`` the same step with the key pass storing no dS and
+the fused query pass recomputing it (no workspace), timed separately.
 
 ``--impl reference`` times the oracle (the CPU reference of this method) on
 the same workload, one bounded sample per step, and prints the same line
@@ -384,6 +387,47 @@ def run_ours(args, w, world, rank, local):
                    h2d_bytes_per_step=host.input_bytes(), d2h_bytes_per_step=host.output_bytes(),
                    steps=Ke, ms_per_step=e_ms / Ke)
 
+    # ---- the same step with the fused query pass (no dS workspace) ----
+    variant = None
+    if not args.no_variants:
+        fbufs = api.Buffers(s, dev, workspace=False)
+        fcalls = (
+            ("fwd", lambda: api.attn_fwd(s, q, k, vt, fbufs.o, fbufs.lse, stream)),
+            ("row_terms", lambda: api.attn_row_terms(s, fbufs.o, dout, fbufs.delta, stream)),
+            ("keys_nostore", lambda: api.attn_bwd_keys(s, q, k, vt, dout, fbufs.lse, fbufs.delta,
+                                                       None, fbufs.dk, fbufs.dvt, stream)),
+            ("queries_fused", lambda: api.attn_bwd_queries_fused(
+                s, q, k, vt, dout, fbufs.lse, fbufs.delta, fbufs.dq, stream)),
+        )
+        for _ in range(args.warmup):
+            flush.zero_()
+            for _, fn in fcalls:
+                fn()
+        Kf = max(1, min(K, 100))
+        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fcalls) + 1)]
+               for _ in range(Kf)]
+        dist_barrier(world)
+        torch.cuda.synchronize(dev)
+        for i in range(Kf):
+            flush.zero_()
+            fev[i][0].record(stream)
+            for c, (_, fn) in enumerate(fcalls):
+                fn()
+                fev[i][c + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        dist_barrier(world)
+        if api.last_device_error(stream) != 0:
+            raise RuntimeError("device error during the fused-dQ steps")
+        f_ms = dist_max(sum(fev[i][0].elapsed_time(fev[i][-1]) for i in range(Kf)), world)
+        variant = dict(
+            what="attn_bwd_keys without the dS store, then attn_bwd_queries_fused (S, P, dP "
+                 "recomputed; no workspace)",
+            value=world * fl["step"] * Kf / (f_ms / 1e3) / 1e12, unit="TFLOP/s", steps=Kf,
+            ms_per_step=f_ms / Kf,
+            kernels_ms={n: sum(fev[i][c].elapsed_time(fev[i][c + 1]) for i in range(Kf)) / Kf
+                        for c, (n, _) in enumerate(fcalls)})
+        del fbufs
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, heads, secs, threads = cpu_oracle_sample(w, inp, args.cpu_budget)
@@ -399,7 +443,8 @@ def run_ours(args, w, world, rank, local):
                     parallelism="replicas" if world > 1 else "single",
                     frac_of_peak=value / world / peaks["tflops"],
                     gpu_launches=len(calls) * K, kernels=kernels, roofline=roof,
-                    clocks=clk, e2e=e2e, cpu_baseline=cpu, wall_s_timed=t_wall)
+                    clocks=clk, e2e=e2e, cpu_baseline=cpu, fused_dq_variant=variant,
+                    wall_s_timed=t_wall)
         print(json.dumps(line))
     return 0
 
@@ -413,6 +458,8 @@ def main():
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip timing the fused-dQ variant of the step")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for cpu_baseline")
     args = ap.parse_args()

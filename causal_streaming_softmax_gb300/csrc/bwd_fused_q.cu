@@ -11,23 +11,24 @@
 // traffic grow as T^2: the key pass then runs without storing dS.
 //
 // GB300 design.
-//   warps 0-7   score gradients, thread = query row (tensor-memory lane);
-//               warps 0-3 take keys 0-63 of a key tile, warps 4-7 keys 64-127,
-//               each in two chunks of 32
-//   warp 8      TMA producer: Q and dO once, then per key tile K and V^T
+//   warps 0-15  score gradients, thread = query row (tensor-memory lane);
+//               warp group w (warps 4w..4w+3) takes keys 32w..32w+31 of a key
+//               tile (sixteen warps measured 10% faster than eight warps of
+//               two 32-key chunks each)
+//   warp 16     TMA producer: Q and dO once, then per key tile K and V^T
 //               through a 4-stage ring
-//   warps 9-11  MMA issuers: S = Q K^T, dP = dO V^T (A = Q / dO copied into
+//   warps 17-19 MMA issuers: S = Q K^T, dP = dO V^T (A = Q / dO copied into
 //               tensor memory once, B = the K tile K-major / the V^T tile as
 //               an MN-major V), dQ += dS K (A = dS from tensor memory, B = the
 //               K tile MN-major)
 // A query row's L and D are per-thread scalars.  The S and dP buffer is
-// released once the score-gradient warps hold its last chunk in registers,
+// released once the score-gradient warps hold their columns in registers,
 // so the next tile's products run during their arithmetic; dS goes into one
 // of two pair buffers, which gives dQ += dS K a tile to finish.
 //
 // Tensor memory (512 columns): Q 0-31, dO 32-63 (binary16 pairs); S 64-191,
-// dP 192-319; dS pair buffer b at 320+64b (keys 0-63 in its first 32
-// columns, 64-127 in the next 32); dQ 448-511.
+// dP 192-319; dS pair buffer b at 320+64b (keys 2i, 2i+1 in column i);
+// dQ 448-511, columns 16w..16w+15 read back by warp group w.
 #include <math.h>
 
 #include <mutex>
@@ -40,7 +41,7 @@ namespace {
 
 constexpr int kBM = 128;  // queries per CTA
 constexpr int kBN = 128;  // keys per tile
-constexpr int kThreads = 384;
+constexpr int kThreads = 640;
 constexpr int kStages = 4;
 constexpr uint32_t kSmemQ = 0, kSmemDO = 16384;
 constexpr uint32_t kSmemStage0 = 32768;
@@ -62,8 +63,8 @@ enum {
   BAR_KV_FULL,                          // [stage] K and V^T landed
   BAR_KV_EMPTY = BAR_KV_FULL + kStages, // [stage] dQ += dS K of the tile done
   BAR_S_FULL = BAR_KV_EMPTY + kStages,  // S and dP of the tile done (2 commits)
-  BAR_LOADED,                           // S and dP are in registers (256 threads)
-  BAR_P_READY,                          // [2] dS of pair buffer b written (256 threads)
+  BAR_LOADED,                           // S and dP are in registers (512 threads)
+  BAR_P_READY,                          // [2] dS of pair buffer b written (512 threads)
   BAR_PK_FREE = BAR_P_READY + 2,        // [2] dQ += dS K has read pair buffer b
   BAR_DONE = BAR_PK_FREE + 2,           // dQ complete
   BAR_COUNT
@@ -109,7 +110,7 @@ __device__ __forceinline__ void score_gradients(const uint32_t (&sv)[32], const 
   }
 }
 
-// 12 warps on four schedulers allow 168 registers a thread.
+// 20 warps on four schedulers allow 96 registers a thread.
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_fused_q_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -153,21 +154,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(BAR_KV_EMPTY + s), 1);
     }
     mbar_init(BAR(BAR_S_FULL), 2);
-    mbar_init(BAR(BAR_LOADED), 256);
+    mbar_init(BAR(BAR_LOADED), 512);
     for (int u = 0; u < 2; ++u) {
-      mbar_init(BAR(BAR_P_READY + u), 256);
+      mbar_init(BAR(BAR_P_READY + u), 512);
       mbar_init(BAR(BAR_PK_FREE + u), 1);
     }
     mbar_init(BAR(BAR_DONE), 1);
     fence_mbarrier_init();
   }
-  if (warp == 9) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+  if (warp == 17) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  if (warp == 8) {
+  if (warp == 16) {
     // ---------------- TMA producer ----------------
     if (lane == 0 && n_kt > 0) {
       tma_prefetch_desc(&tm_q);
@@ -194,9 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
         drain_wait(BAR(BAR_KV_FULL + j % kStages), (j / kStages) & 1, a.wait_ns);
     }
-  } else if (warp >= 9) {
+  } else if (warp >= 17) {
     // ---------------- MMA issuers ----------------
-    const int role = warp - 9;  // 0: S = Q K^T, 1: dP = dO V^T, 2: dQ += dS K
+    const int role = warp - 17;  // 0: S = Q K^T, 1: dP = dO V^T, 2: dQ += dS K
     if (lane == 0 && n_kt > 0) {
       bool ok = true;
       if (role < 2) {
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- score gradients: thread = query row ----------------
-    const int wg = warp >> 2;  // keys 64wg..64wg+63 of each tile
+    const int wg = warp >> 2;  // keys 32wg..32wg+31 of each tile
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int q = q0 + r;
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       D = a.delta[lrow];
     }
     bool ok = true;
-    if (n_kt > 0) {
+    if (n_kt > 0 && wg < 2) {
       // Q (warps 0-3) or dO (warps 4-7) row r into tensor memory as A operands
       ok = mbar_wait_warp(BAR(BAR_QD_FULL), 0, wc);
       uint32_t w[32];
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int j = 0; ok && j < n_kt; ++j) {
       const int pb = j & 1;
-      const int k0 = j * kBN + 64 * wg;  // this thread's first key
+      const int k0 = j * kBN + 32 * wg;  // this thread's first key
       if (!mbar_wait_warp(BAR(BAR_S_FULL), j & 1, wc)) {
         ok = false;
         break;
@@ -288,24 +289,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-#pragma unroll 1
-      for (int ch = 0; ch < 2; ++ch) {
+      {
         uint32_t sv[32], dv[32];
-        const uint32_t col = 64 * wg + 32 * ch;
+        const uint32_t col = 32 * wg;
         tmem_ld32x2_wait(tmem + lane_base + kColS + col, tmem + lane_base + kColDP + col, sv, dv);
-        if (ch == 1) {
-          // both chunks are in registers: the S and dP buffer is free
-          tc_fence_before();
-          mbar_arrive(BAR(BAR_LOADED));
-        }
-        const int kc = k0 + 32 * ch;
-        const int lim_local = lim - kc;
+        tc_fence_before();
+        mbar_arrive(BAR(BAR_LOADED));
+        const int lim_local = lim - k0;
         uint32_t dd[16];
         if (lim_local < 32)
           score_gradients<true>(sv, dv, c, L, D, lim_local, dd);
         else
           score_gradients<false>(sv, dv, c, L, D, lim_local, dd);
-        tmem_st16(tmem + lane_base + kColDS + 64 * pb + 32 * wg + 16 * ch, dd);
+        tmem_st16(tmem + lane_base + kColDS + 64 * pb + 16 * wg, dd);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -314,35 +310,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------- epilogue: dQ = s * sum; warp group w takes columns 32w.. ----------------
     if (q < T) {
-      float* dst = a.dq + lrow * 64 + 32 * wg;
+      float* dst = a.dq + lrow * 64 + 16 * wg;
       if (n_kt > 0) {
         ok = mbar_wait_warp(BAR(BAR_DONE), 0, wc) && ok;
         tc_fence_after();
-        uint32_t r0[32];
-        tmem_ld32_wait(tmem + lane_base + kColDQ + 32 * wg, r0);
+        uint32_t r0[16];
+        tmem_ld16_wait(tmem + lane_base + kColDQ + 16 * wg, r0);
         float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
+        for (int u = 0; u < 4; ++u)
           d4[u] = make_float4(as_f(r0[4 * u]) * d.scale, as_f(r0[4 * u + 1]) * d.scale,
                               as_f(r0[4 * u + 2]) * d.scale, as_f(r0[4 * u + 3]) * d.scale);
       } else {
         float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) d4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < 4; ++u) d4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     } else if (n_kt > 0) {
-      // rows past T still take part in the warp-wide tensor-memory load
       ok = mbar_wait_warp(BAR(BAR_DONE), 0, wc) && ok;
       tc_fence_after();
-      uint32_t r0[32];
-      tmem_ld32_wait(tmem + lane_base + kColDQ + 32 * wg, r0);
+      uint32_t r0[16];
+      tmem_ld16_wait(tmem + lane_base + kColDQ + 16 * wg, r0);
     }
     (void)ok;
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 17) {
     tc_fence_after();
     if (n_kt > 0) drain_wait(BAR(BAR_DONE), 0, a.wait_ns);
     __syncwarp();
