@@ -2,9 +2,10 @@
 // query head per CTA, with S, P, dP and dS recomputed from Q, K, V, dO, L and
 // D instead of read back from a stored dS.
 //
-// Method (StreamingAttentionSM86.alpha, the query-side backward: the page-2
-// pass that forms S, P and dP again for a query tile and accumulates
-// dQ = s * sum_j dS_j K_j over the visible key tiles):
+// Method (StreamingAttentionSM86.alpha, backward-pass header: the query
+// launch streamingAttentionQuerySM86, which walks a query tile's key tiles up
+// to the diagonal as the forward does, forms P, dP and dS again and keeps
+// dQ = s * sum_j dS_j K_j):
 //   S = Q K^T, P = 2^(S c - L), dP = dO V^T, dS = P (dP - D), dQ += dS K,
 // dS rounded to binary16 before its product, as in the key pass.  It trades
 // two recomputed products per tile pair for the dS workspace, whose size and

@@ -158,9 +158,9 @@ ATTN_API int attn_bwd_queries(const attn_shape* shape, const uint16_t* k,
                      void* stream);
 
 /*
- * Fused query pass (the page-2 query-side backward of
- * StreamingAttentionSM86.alpha, which forms S, P and dP again for a query
- * tile): for each 128-query block, S = Q K^T, P = 2^(S c - L),
+ * Fused query pass (the query launch streamingAttentionQuerySM86 of
+ * StreamingAttentionSM86.alpha, backward-pass header, which walks a query
+ * tile's key tiles and forms S, P and dP again): for each 128-query block, S = Q K^T, P = 2^(S c - L),
  * dP = dO V^T and dS = P (dP - D) are recomputed for every visible key block
  * and dQ = s * sum of dS K is accumulated; dS is rounded to binary16 before
  * its product, as in the key pass.  Needs no workspace: pair it with
