@@ -342,11 +342,14 @@ def attn_step_host(s: Shape, host: HostProblem, dev_in: DeviceInputs, bufs: Buff
     """Host-to-host pass through the C ABI: copies the inputs in, runs the
     four calls and copies O, L, dQ, dK and dV^T back, the copies overlapped
     with the kernels (asynchronous; synchronise the stream before reading
-    ``host``'s outputs)."""
+    ``host``'s outputs).  ``bufs`` without a workspace selects the fused
+    query pass."""
     dev = AttnDeviceBuffers(dev_in.q.data_ptr(), dev_in.k.data_ptr(), dev_in.vt.data_ptr(),
                             dev_in.dout.data_ptr(), bufs.o.data_ptr(), bufs.lse.data_ptr(),
-                            bufs.delta.data_ptr(), bufs.ws.data_ptr(),
-                            bufs.ws.numel() * bufs.ws.element_size(), bufs.dq.data_ptr(),
+                            bufs.delta.data_ptr(),
+                            None if bufs.ws is None else bufs.ws.data_ptr(),
+                            0 if bufs.ws is None else bufs.ws.numel() * bufs.ws.element_size(),
+                            bufs.dq.data_ptr(),
                             bufs.dk.data_ptr(), bufs.dvt.data_ptr())
     shape = s.c_struct()
     _check("attn_step_host", load_library().attn_step_host(

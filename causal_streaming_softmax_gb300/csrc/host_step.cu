@@ -2,7 +2,8 @@
 // memory to host memory, with the copies overlapped with the kernels.
 //
 // The kernels run in order on the caller's stream: forward, row terms, key
-// pass, then the dQ pass in two K/V-head halves.  A second stream, owned by
+// pass, then the dQ pass in two K/V-head halves (the fused query pass when
+// the caller gives no workspace, the key pass then storing no dS).  A second stream, owned by
 // the library (one per device), carries the copies that need not wait for
 // the whole chain:
 //   dO goes in after Q, K and V^T (so it never slows their copy) while the
@@ -68,15 +69,17 @@ extern "C" ATTN_API int attn_step_host(const attn_shape* shape, const attn_devic
   if (d.kv_begin != 0 || d.kv_count != d.Hkv) return ATTN_ERR_SHAPE;  // whole problems only
   if (!dev || !h_q || !h_k || !h_vt || !h_dout || !h_o || !h_lse || !h_dq || !h_dk || !h_dvt)
     return ATTN_ERR_NULL;
+  // no workspace (null, 0 bytes): the fused query pass recomputes dS
+  const bool fused = dev->ws == nullptr && dev->ws_bytes == 0;
   if (!dev->q || !dev->k || !dev->vt || !dev->dout || !dev->o || !dev->lse || !dev->delta ||
-      !dev->ws || !dev->dq || !dev->dk || !dev->dvt)
+      (!fused && !dev->ws) || !dev->dq || !dev->dk || !dev->dvt)
     return ATTN_ERR_NULL;
   if (!aligned16(dev->q) || !aligned16(dev->k) || !aligned16(dev->vt) ||
       !aligned16(dev->dout) || !aligned16(dev->o) || !aligned16(dev->lse) ||
       !aligned16(dev->delta) || !aligned16(dev->ws) || !aligned16(dev->dq) ||
       !aligned16(dev->dk) || !aligned16(dev->dvt))
     return ATTN_ERR_ALIGN;
-  if (dev->ws_bytes < workspace_bytes_for(d)) return ATTN_ERR_WORKSPACE;
+  if (!fused && dev->ws_bytes < workspace_bytes_for(d)) return ATTN_ERR_WORKSPACE;
   DevCtx ctx;
   if ((rc = device_context(&ctx)) != ATTN_OK) return rc;
   int device = 0;
@@ -139,7 +142,11 @@ extern "C" ATTN_API int attn_step_host(const attn_shape* shape, const attn_devic
     c.kv_count = (d.Hkv * (part + 1)) / halves - kv0;
     c.ws_heads = d.H;
     c.ws_h0 = kv0 * d.G;
-    RC(launch_bwd_queries(c, ctx, dev->k, ws, dev->dq, main));
+    if (fused)
+      RC(launch_bwd_fused_q(c, ctx, dev->q, dev->k, dev->vt, dev->dout, dev->lse, dev->delta,
+                            dev->dq, main));
+    else
+      RC(launch_bwd_queries(c, ctx, dev->k, ws, dev->dq, main));
     if (part + 1 < halves) {
       CK(cudaEventRecord(ev[4], main));
       CK(cudaStreamWaitEvent(side, ev[4], 0));

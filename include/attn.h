@@ -181,7 +181,8 @@ ATTN_API int attn_bwd_queries_fused(const attn_shape* shape, const uint16_t* q,
  * q, dout [B][H][T][64] and k [B][Hkv][T][64], vt [B][Hkv][64][T] (binary16);
  * o [B][T][H*64] (binary16); lse, delta [B][H][T]; dq [B][H][T][64],
  * dk [B][Hkv][T][64], dvt [B][Hkv][64][T] (binary32); ws the dS workspace of
- * ws_bytes >= attn_bwd_workspace_bytes.  Owned by the caller.
+ * ws_bytes >= attn_bwd_workspace_bytes, or NULL with 0 bytes (attn_step_host
+ * then uses the fused query pass).  Owned by the caller.
  */
 typedef struct attn_device_buffers {
   uint16_t* q;
@@ -214,7 +215,8 @@ typedef struct attn_device_buffers {
  * before then.  Host buffers should be page-locked (pageable memory works,
  * but its copies do not overlap).  The shape must cover every K/V head
  * (head_begin = 0, head_count = 0 or Hkv); seq_lens, if any, is a device
- * array.  Errors as the calls above; a CUDA failure while enqueueing
+ * array.  With dev->ws = NULL and dev->ws_bytes = 0 the step takes dQ from
+ * attn_bwd_queries_fused and the key pass stores no dS (no workspace).  Errors as the calls above; a CUDA failure while enqueueing
  * returns ATTN_ERR_CUDA with the work enqueued so far left on the streams.
  */
 ATTN_API int attn_step_host(const attn_shape* shape, const attn_device_buffers* dev,

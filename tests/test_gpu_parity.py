@@ -204,23 +204,25 @@ def test_workload_sampled(cuda_device, cfg):
     _check_sampled(w, inp, gpu, heads, kv_heads, batches, rng)
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("B,T,H,Hkv,causal,lens", [
     (1, 512, 8, 2, True, None),
     (3, 384, 4, 2, False, [100, 384, 257]),   # batches: the split dQ copy is strided
     (2, 256, 2, 1, True, None),               # one K/V head: dQ in one piece
 ])
-def test_step_host_matches_device_path(cuda_device, B, T, H, Hkv, causal, lens):
+def test_step_host_matches_device_path(cuda_device, B, T, H, Hkv, causal, lens, fused):
     """attn_step_host (host buffers in and out, copies overlapped with the
-    kernels) gives the same bits as the four device calls."""
+    kernels) gives the same bits as the four device calls, with the stored
+    or the fused dQ pass."""
     import torch
     from causal_streaming_softmax_gb300 import api
     inp = workloads.make_custom_inputs(B, T, H, Hkv, causal=causal, lens=lens, seed=T + B)
-    ref = run_gpu(inp, causal=causal)
+    ref = run_gpu(inp, causal=causal, fused_dq=fused)
     ln = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
     s = api.Shape(B, T, H, Hkv, causal=causal, seq_lens=ln)
     host = api.HostProblem(s, *(torch.from_numpy(inp[n]) for n in ("q", "k", "vt", "dout")))
     dev_in = api.DeviceInputs(s)
-    bufs = api.Buffers(s)
+    bufs = api.Buffers(s, workspace=not fused)
     for out in (host.o, host.lse, host.dq, host.dk, host.dvt):
         out.fill_(float("nan"))
     stream = torch.cuda.Stream()
@@ -284,3 +286,26 @@ def test_fused_dq_workload_sampled(cuda_device, cfg):
     rng = np.random.default_rng(200 + cfg)
     G = w.group
     _check_sampled(w, inp, gpu, [0, G - 1, w.heads - 1], [w.kv_heads - 1], [0], rng)
+
+
+def test_fused_dq_head_chunks_match_whole(cuda_device):
+    """The fused query pass walked in K/V-head chunks gives the same bits as
+    one call over every head."""
+    import torch
+    from causal_streaming_softmax_gb300 import api
+    inp = workloads.make_custom_inputs(2, 384, 8, 4, causal=True, lens=[200, 384], seed=19)
+    whole = run_gpu(inp, causal=True, fused_dq=True)
+    dev = "cuda"
+    q, k, vt, dout = (torch.from_numpy(inp[n]).to(dev) for n in ("q", "k", "vt", "dout"))
+    ln = torch.tensor([200, 384], dtype=torch.int32, device=dev)
+    s = api.Shape(2, 384, 8, 4, causal=True, seq_lens=ln)
+    bufs = api.Buffers(s, workspace=False)
+    api.attn_fwd(s, q, k, vt, bufs.o, bufs.lse)
+    api.attn_row_terms(s, bufs.o, dout, bufs.delta)
+    bufs.dq.fill_(float("nan"))
+    for begin, count in ((0, 1), (1, 2), (3, 1)):
+        api.attn_bwd_queries_fused(s.chunk(begin, count), q, k, vt, dout, bufs.lse, bufs.delta,
+                                   bufs.dq)
+    torch.cuda.synchronize()
+    assert api.last_device_error() == 0
+    assert np.array_equal(bufs.dq.cpu().numpy(), whole["dq"])
