@@ -27,9 +27,11 @@
 // two steps to finish.  With those latencies off the loop, a step costs the
 // score-gradient work.  The four product chains are issued by four warps.
 // dK and dV sum the group's query heads in tensor memory (no atomics, fixed
-// order).  dS^T also goes to shared memory in the 128-byte-swizzled image
-// the dQ pass reads; the store warp copies it into the workspace, so no
-// score-gradient warp ever waits for a store.
+// order).  dS^T also goes to shared memory (three buffers) in the
+// 128-byte-swizzled image the dQ pass reads; the store warp copies it into
+// the workspace, so no score-gradient warp ever waits for a store.  Without a
+// workspace (the fused query pass recomputes dS) the staging and the store
+// are skipped.
 //
 // Tensor memory (512 columns): K 0-31, V 32-63 (binary16 pairs), S^T 64-127,
 // dP^T 128-191; pair buffer b at 192+64b: P^T of queries 32w..32w+31 at
