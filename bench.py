@@ -19,8 +19,9 @@ four kernels, device -> host copies of O, L, dQ, dK, dV^T, all inside the
 timed region, the copies overlapped with the kernels),
 ``roofline`` the dominant kernel against the measured tensor peak,
 ``cpu_baseline`` the binary64 oracle on a bounded sample timed on the host,
-and ``fused_dq_variant`` the same step with the key pass storing no dS and
-the fused query pass recomputing it (no workspace), timed separately.
+and ``fused_dq_variant`` the same step as the pages' two-launch backward:
+the fused query pass (D and dQ, recomputing S, P, dP) then the key pass
+storing no dS (no workspace), timed separately.
 
 ``--impl reference`` times the oracle (the CPU reference of this method) on
 the same workload, one bounded sample per step, and prints the same line
@@ -393,11 +394,10 @@ def run_ours(args, w, world, rank, local):
         fbufs = api.Buffers(s, dev, workspace=False)
         fcalls = (
             ("fwd", lambda: api.attn_fwd(s, q, k, vt, fbufs.o, fbufs.lse, stream)),
-            ("row_terms", lambda: api.attn_row_terms(s, fbufs.o, dout, fbufs.delta, stream)),
+            ("queries_fused", lambda: api.attn_bwd_queries_fused(
+                s, q, k, vt, dout, fbufs.o, fbufs.lse, fbufs.delta, fbufs.dq, stream)),
             ("keys_nostore", lambda: api.attn_bwd_keys(s, q, k, vt, dout, fbufs.lse, fbufs.delta,
                                                        None, fbufs.dk, fbufs.dvt, stream)),
-            ("queries_fused", lambda: api.attn_bwd_queries_fused(
-                s, q, k, vt, dout, fbufs.lse, fbufs.delta, fbufs.dq, stream)),
         )
         for _ in range(args.warmup):
             flush.zero_()
@@ -420,8 +420,8 @@ def run_ours(args, w, world, rank, local):
             raise RuntimeError("device error during the fused-dQ steps")
         f_ms = dist_max(sum(fev[i][0].elapsed_time(fev[i][-1]) for i in range(Kf)), world)
         variant = dict(
-            what="attn_bwd_keys without the dS store, then attn_bwd_queries_fused (S, P, dP "
-                 "recomputed; no workspace)",
+            what="attn_fwd, attn_bwd_queries_fused (D and dQ, S, P, dP recomputed), then "
+                 "attn_bwd_keys storing no dS: no workspace, no row-terms launch",
             value=world * fl["step"] * Kf / (f_ms / 1e3) / 1e12, unit="TFLOP/s", steps=Kf,
             ms_per_step=f_ms / Kf,
             kernels_ms={n: sum(fev[i][c].elapsed_time(fev[i][c + 1]) for i in range(Kf)) / Kf

@@ -75,7 +75,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attn_bwd_workspace_bytes.restype = sz
     lib.attn_bwd_keys.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     lib.attn_bwd_queries.argtypes = [sp, vp, vp, sz, vp, vp]
-    lib.attn_bwd_queries_fused.argtypes = [sp] + [vp] * 8
+    lib.attn_bwd_queries_fused.argtypes = [sp] + [vp] * 9
     lib.attn_bwd_queries_fused.restype = ctypes.c_int
     lib.attn_error_string.argtypes = [ctypes.c_int]
     lib.attn_error_string.restype = ctypes.c_char_p
@@ -228,12 +228,14 @@ def attn_bwd_queries(s: Shape, k, ws, dq, stream=None) -> None:
            load_library().attn_bwd_queries(ctypes.byref(shape), *args, _stream_ptr(stream)))
 
 
-def attn_bwd_queries_fused(s: Shape, q, k, vt, dout, lse, delta, dq, stream=None) -> None:
+def attn_bwd_queries_fused(s: Shape, q, k, vt, dout, o, lse, delta, dq, stream=None) -> None:
+    """Writes ``delta`` (D = rowsum(dO * O)) and ``dq``; replaces attn_row_terms."""
     B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
     args = (_want(q, "q", torch.float16, (B, H, T, 64)),
             _want(k, "k", torch.float16, (B, Hkv, T, 64)),
             _want(vt, "vt", torch.float16, (B, Hkv, 64, T)),
             _want(dout, "dout", torch.float16, (B, H, T, 64)),
+            _want(o, "o", torch.float16, (B, T, H * 64)),
             _want(lse, "lse", torch.float32, (B, H, T)),
             _want(delta, "delta", torch.float32, (B, H, T)),
             _want(dq, "dq", torch.float32, (B, H, T, 64)))
@@ -290,14 +292,15 @@ class Buffers:
 def forward_backward(s: Shape, q, k, vt, dout, bufs: Buffers, stream=None,
                      fused_dq: bool = False) -> Buffers:
     """One pass of the whole path: attn_fwd, attn_row_terms, attn_bwd_keys,
-    attn_bwd_queries; with ``fused_dq`` the key pass stores no dS and
-    attn_bwd_queries_fused recomputes it (``bufs.ws`` unused)."""
+    attn_bwd_queries; with ``fused_dq``: attn_fwd, attn_bwd_queries_fused
+    (D and dQ, S, P, dP recomputed), then attn_bwd_keys storing no dS
+    (``bufs.ws`` unused)."""
     attn_fwd(s, q, k, vt, bufs.o, bufs.lse, stream)
-    attn_row_terms(s, bufs.o, dout, bufs.delta, stream)
     if fused_dq:
+        attn_bwd_queries_fused(s, q, k, vt, dout, bufs.o, bufs.lse, bufs.delta, bufs.dq, stream)
         attn_bwd_keys(s, q, k, vt, dout, bufs.lse, bufs.delta, None, bufs.dk, bufs.dvt, stream)
-        attn_bwd_queries_fused(s, q, k, vt, dout, bufs.lse, bufs.delta, bufs.dq, stream)
     else:
+        attn_row_terms(s, bufs.o, dout, bufs.delta, stream)
         attn_bwd_keys(s, q, k, vt, dout, bufs.lse, bufs.delta, bufs.ws, bufs.dk, bufs.dvt,
                       stream)
         attn_bwd_queries(s, k, bufs.ws, bufs.dq, stream)

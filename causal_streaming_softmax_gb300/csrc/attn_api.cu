@@ -226,18 +226,18 @@ int attn_bwd_keys(const attn_shape* shape, const uint16_t* q, const uint16_t* k,
 }
 
 int attn_bwd_queries_fused(const attn_shape* shape, const uint16_t* q, const uint16_t* k,
-                           const uint16_t* vt, const uint16_t* dout, const float* lse,
-                           const float* delta, float* dq, void* stream) {
+                           const uint16_t* vt, const uint16_t* dout, const uint16_t* o,
+                           const float* lse, float* delta, float* dq, void* stream) {
   Dims d;
   int rc = validate_shape(shape, &d);
   if (rc != ATTN_OK) return rc;
-  if (!q || !k || !vt || !dout || !lse || !delta || !dq) return ATTN_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(dout) || !aligned16(lse) ||
-      !aligned16(delta) || !aligned16(dq))
+  if (!q || !k || !vt || !dout || !o || !lse || !delta || !dq) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(dout) || !aligned16(o) ||
+      !aligned16(lse) || !aligned16(delta) || !aligned16(dq))
     return ATTN_ERR_ALIGN;
   DevCtx ctx;
   if ((rc = device_context(&ctx)) != ATTN_OK) return rc;
-  return launch_bwd_fused_q(d, ctx, q, k, vt, dout, lse, delta, dq,
+  return launch_bwd_fused_q(d, ctx, q, k, vt, dout, o, lse, delta, dq,
                             static_cast<cudaStream_t>(stream));
 }
 

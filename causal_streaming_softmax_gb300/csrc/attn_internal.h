@@ -69,8 +69,8 @@ int launch_bwd_keys(const Dims& d, const DevCtx& ctx, const uint16_t* q, const u
                     const float* delta, uint8_t* ws, float* dk, float* dvt,
                     cudaStream_t stream);
 int launch_bwd_fused_q(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16_t* k,
-                       const uint16_t* vt, const uint16_t* dout, const float* lse,
-                       const float* delta, float* dq, cudaStream_t stream);
+                       const uint16_t* vt, const uint16_t* dout, const uint16_t* o,
+                       const float* lse, float* delta, float* dq, cudaStream_t stream);
 int launch_bwd_queries(const Dims& d, const DevCtx& ctx, const uint16_t* k, const uint8_t* ws,
                        float* dq, cudaStream_t stream);
 int launch_wait_probe(const DevCtx& ctx, uint64_t limit_ns, cudaStream_t stream);

@@ -3,10 +3,12 @@
 // D instead of read back from a stored dS.
 //
 // Method (StreamingAttentionSM86.alpha, backward-pass header: the query
-// launch streamingAttentionQuerySM86, which walks a query tile's key tiles up
-// to the diagonal as the forward does, forms P, dP and dS again and keeps
-// dQ = s * sum_j dS_j K_j):
-//   S = Q K^T, P = 2^(S c - L), dP = dO V^T, dS = P (dP - D), dQ += dS K,
+// launch streamingAttentionQuerySM86, which forms D for its rows from dO and
+// the forward's O, writes it for the key launch, then walks the query tile's
+// key tiles up to the diagonal as the forward does, forms P, dP and dS again
+// and keeps dQ = s * sum_j dS_j K_j):
+//   D = rowsum(dO * O), S = Q K^T, P = 2^(S c - L), dP = dO V^T,
+//   dS = P (dP - D), dQ += dS K,
 // dS rounded to binary16 before its product, as in the key pass.  It trades
 // two recomputed products per tile pair for the dS workspace, whose size and
 // traffic grow as T^2: the key pass then runs without storing dS.
@@ -22,7 +24,9 @@
 //               tensor memory once, B = the K tile K-major / the V^T tile as
 //               an MN-major V), dQ += dS K (A = dS from tensor memory, B = the
 //               K tile MN-major)
-// A query row's L and D are per-thread scalars.  The S and dP buffer is
+// A query row's L and D are per-thread scalars; warps 4-7, which copy dO
+// into tensor memory, form D from it and the row's O (binary16 widened,
+// binary32 sum) and hand it to the other warps through shared memory.  The S and dP buffer is
 // released once the score-gradient warps hold their columns in registers,
 // so the next tile's products run during their arithmetic; dS goes into one
 // of two pair buffers, which gives dQ += dS K a tile to finish.
@@ -60,7 +64,7 @@ constexpr uint32_t kIdescDQ = idesc_f16_f32(128, 64, 0, 1);   // dS (tmem) x K (
 
 enum {
   BAR_QD_FULL = 0,                      // Q and dO tiles landed
-  BAR_QD_TMEM,                          // Q and dO in tensor memory (256 threads)
+  BAR_QD_TMEM,                          // Q, dO in tensor memory, D in shared (256 threads)
   BAR_KV_FULL,                          // [stage] K and V^T landed
   BAR_KV_EMPTY = BAR_KV_FULL + kStages, // [stage] dQ += dS K of the tile done
   BAR_S_FULL = BAR_KV_EMPTY + kStages,  // S and dP of the tile done (2 commits)
@@ -74,8 +78,9 @@ static_assert(BAR_COUNT * 8 <= 256, "barrier area");
 
 struct FusedArgs {
   Dims d;
+  const uint16_t* o;
   const float* lse;
-  const float* delta;
+  float* delta;
   float* dq;
   uint32_t* err;
   uint64_t wait_ns;
@@ -120,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ float s_D[kBM];
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const sgen = smem_raw + (sbase - smem_u32(smem_raw));
@@ -256,13 +262,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     int lim = row_ok ? len : 0;
     if (d.causal) lim = min(lim, q + 1);
     const size_t lrow = ((size_t)b * d.H + h) * T + q;
-    float L = 0.f, D = 0.f;
-    if (row_ok) {
-      L = a.lse[lrow];
-      D = a.delta[lrow];
-    }
+    const float L = row_ok ? a.lse[lrow] : 0.f;
     bool ok = true;
     if (n_kt > 0 && wg < 2) {
+      // the row's O for D, loaded while Q and dO are on their way
+      uint4 ov[8];
+      if (wg == 1 && row_ok) {
+        const uint4* orow =
+            reinterpret_cast<const uint4*>(a.o + (((size_t)b * T + q) * d.H + h) * 64);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) ov[ch] = __ldg(orow + ch);
+      }
       // Q (warps 0-3) or dO (warps 4-7) row r into tensor memory as A operands
       ok = mbar_wait_warp(BAR(BAR_QD_FULL), 0, wc);
       uint32_t w[32];
@@ -273,10 +283,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         w[4 * ch] = v.x, w[4 * ch + 1] = v.y, w[4 * ch + 2] = v.z, w[4 * ch + 3] = v.w;
       }
       tmem_st32(tmem + lane_base + (wg == 0 ? kColQ : kColDO), w);
+      if (wg == 1) {
+        // row terms D = rowsum(dO * O) from the stored binary16 O
+        float D = 0.f;
+        if (row_ok) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};  // four chains, summed at the end
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint32_t ow[4] = {ov[ch].x, ov[ch].y, ov[ch].z, ov[ch].w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t dw = w[4 * ch + u];
+              acc[u] = fmaf(f16_bits_to_f32((uint16_t)(dw & 0xFFFFu)),
+                            f16_bits_to_f32((uint16_t)(ow[u] & 0xFFFFu)), acc[u]);
+              acc[u] = fmaf(f16_bits_to_f32((uint16_t)(dw >> 16)),
+                            f16_bits_to_f32((uint16_t)(ow[u] >> 16)), acc[u]);
+            }
+          }
+          D = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        }
+        s_D[r] = D;
+        if (q < T) a.delta[lrow] = D;
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(BAR(BAR_QD_TMEM));
+    } else if (n_kt == 0 && wg == 1 && q < T) {
+      a.delta[lrow] = 0.f;  // no row of this tile sees a key
     }
+    // every score-gradient warp takes its row's D from shared memory
+    if (n_kt > 0 && !mbar_wait_warp(BAR(BAR_QD_TMEM), 0, wc)) ok = false;
+    const float D = n_kt > 0 ? s_D[r] : 0.f;
     for (int j = 0; ok && j < n_kt; ++j) {
       const int pb = j & 1;
       const int k0 = j * kBN + 32 * wg;  // this thread's first key
@@ -350,8 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int launch_bwd_fused_q(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16_t* k,
-                       const uint16_t* vt, const uint16_t* dout, const float* lse,
-                       const float* delta, float* dq, cudaStream_t stream) {
+                       const uint16_t* vt, const uint16_t* dout, const uint16_t* o,
+                       const float* lse, float* delta, float* dq, cudaStream_t stream) {
   CUtensorMap tq, tk, tv, tdo;
   const uint64_t T = (uint64_t)d.T;
   if (!encode_tmap_3d(&tq, q, 64, T, (uint64_t)d.B * d.H, 128, T * 128, 64, kBM) ||
@@ -368,7 +405,7 @@ int launch_bwd_fused_q(const Dims& d, const DevCtx& ctx, const uint16_t* q, cons
         bwd_fused_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr_status[dev & 63] != cudaSuccess) return cuda_status(attr_status[dev & 63]);
-  FusedArgs args{d, lse, delta, dq, ctx.err, ctx.wait_ns};
+  FusedArgs args{d, o, lse, delta, dq, ctx.err, ctx.wait_ns};
   dim3 grid(d.kv_count * d.G, d.nt, d.B);
   bwd_fused_q_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, args);
   return cuda_status(cudaGetLastError());

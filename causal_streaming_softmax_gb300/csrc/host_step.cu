@@ -2,15 +2,15 @@
 // memory to host memory, with the copies overlapped with the kernels.
 //
 // The kernels run in order on the caller's stream: forward, row terms, key
-// pass, then the dQ pass in two K/V-head halves (the fused query pass when
-// the caller gives no workspace, the key pass then storing no dS).  A second stream, owned by
-// the library (one per device), carries the copies that need not wait for
-// the whole chain:
+// pass, then the dQ pass in two K/V-head halves; or, when the caller gives no
+// workspace, forward, the fused query pass in two halves (it forms D), then
+// the key pass storing no dS.  A second stream, owned by the library (one
+// per device), carries the copies that need not wait for the whole chain:
 //   dO goes in after Q, K and V^T (so it never slows their copy) while the
 //   forward runs; O and L come back while the backward runs; dK and dV^T
-//   come back while the dQ pass runs; the first half's dQ comes back while
-//   the second half is computed.  Only Q, K, V^T in and the last dQ half out
-//   are exposed.  The caller's stream waits for the side stream at the end,
+//   come back while the dQ pass runs (stored path); dQ comes back in halves,
+//   each while later kernels run.  Only Q, K, V^T in and the last outputs
+//   out are exposed.  The caller's stream waits for the side stream at the end,
 //   so everything is complete once the caller's stream is.
 #include <mutex>
 
@@ -125,38 +125,47 @@ extern "C" ATTN_API int attn_step_host(const attn_shape* shape, const attn_devic
   CK(cudaMemcpyAsync(h_lse, dev->lse, lse_bytes, d2h, side));
 
   CK(cudaStreamWaitEvent(main, ev[1], 0));
-  RC(launch_row_terms(d, ctx, dev->o, dev->dout, dev->delta, main));
-  RC(launch_bwd_keys(d, ctx, dev->q, dev->k, dev->vt, dev->dout, dev->lse, dev->delta, ws,
-                     dev->dk, dev->dvt, main));
-  CK(cudaEventRecord(ev[3], main));
-  CK(cudaStreamWaitEvent(side, ev[3], 0));
-  CK(cudaMemcpyAsync(h_dk, dev->dk, dk_bytes, d2h, side));
-  CK(cudaMemcpyAsync(h_dvt, dev->dvt, dk_bytes, d2h, side));
-
-  // dQ pass in two K/V-head halves over the whole-problem workspace layout
   const int halves = d.Hkv >= 2 ? 2 : 1;
-  int kv0 = 0;
-  for (int part = 0; part < halves; ++part) {
+  // the dQ pass in two K/V-head halves; the first half's dQ comes back while
+  // the rest of the backward runs
+  auto dq_half = [&](int part, int& kv0, bool last) -> int {
     Dims c = d;
     c.kv_begin = kv0;
     c.kv_count = (d.Hkv * (part + 1)) / halves - kv0;
     c.ws_heads = d.H;
     c.ws_h0 = kv0 * d.G;
-    if (fused)
-      RC(launch_bwd_fused_q(c, ctx, dev->q, dev->k, dev->vt, dev->dout, dev->lse, dev->delta,
-                            dev->dq, main));
-    else
-      RC(launch_bwd_queries(c, ctx, dev->k, ws, dev->dq, main));
-    if (part + 1 < halves) {
-      CK(cudaEventRecord(ev[4], main));
-      CK(cudaStreamWaitEvent(side, ev[4], 0));
-      CK(copy_heads(h_dq, dev->dq, d.B, d.H, c.kv_begin * d.G, c.kv_count * d.G, dq_row, d2h,
-                    side));
-    } else {
-      CK(copy_heads(h_dq, dev->dq, d.B, d.H, c.kv_begin * d.G, c.kv_count * d.G, dq_row, d2h,
-                    main));
+    int r = fused ? launch_bwd_fused_q(c, ctx, dev->q, dev->k, dev->vt, dev->dout, dev->o,
+                                       dev->lse, dev->delta, dev->dq, main)
+                  : launch_bwd_queries(c, ctx, dev->k, ws, dev->dq, main);
+    if (r != ATTN_OK) return r;
+    cudaError_t e;
+    if (!last) {
+      if ((e = cudaEventRecord(ev[4], main)) != cudaSuccess) return cuda_status(e);
+      if ((e = cudaStreamWaitEvent(side, ev[4], 0)) != cudaSuccess) return cuda_status(e);
     }
+    e = copy_heads(h_dq, dev->dq, d.B, d.H, c.kv_begin * d.G, c.kv_count * d.G, dq_row, d2h,
+                   last ? main : side);
+    if (e != cudaSuccess) return cuda_status(e);
     kv0 += c.kv_count;
+    return ATTN_OK;
+  };
+  int kv0 = 0;
+  if (fused) {
+    // the fused query pass forms D itself, then the key pass (no dS store)
+    for (int part = 0; part < halves; ++part) RC(dq_half(part, kv0, false));
+    RC(launch_bwd_keys(d, ctx, dev->q, dev->k, dev->vt, dev->dout, dev->lse, dev->delta,
+                       nullptr, dev->dk, dev->dvt, main));
+    CK(cudaMemcpyAsync(h_dk, dev->dk, dk_bytes, d2h, main));
+    CK(cudaMemcpyAsync(h_dvt, dev->dvt, dk_bytes, d2h, main));
+  } else {
+    RC(launch_row_terms(d, ctx, dev->o, dev->dout, dev->delta, main));
+    RC(launch_bwd_keys(d, ctx, dev->q, dev->k, dev->vt, dev->dout, dev->lse, dev->delta, ws,
+                       dev->dk, dev->dvt, main));
+    CK(cudaEventRecord(ev[3], main));
+    CK(cudaStreamWaitEvent(side, ev[3], 0));
+    CK(cudaMemcpyAsync(h_dk, dev->dk, dk_bytes, d2h, side));
+    CK(cudaMemcpyAsync(h_dvt, dev->dvt, dk_bytes, d2h, side));
+    for (int part = 0; part < halves; ++part) RC(dq_half(part, kv0, part + 1 == halves));
   }
   CK(cudaEventRecord(ev[5], side));
   CK(cudaStreamWaitEvent(main, ev[5], 0));

@@ -138,9 +138,9 @@ ATTN_API size_t attn_bwd_workspace_bytes(const attn_shape* shape);
  * dV += P^T dO and dK += dS^T Q over every query head of the group; dS^T is
  * stored (binary16) into ds_ws.  Writes dk = s * sum and dvt (unscaled) for
  * the chunk's K/V heads.  Needs lse from attn_fwd and delta from
- * attn_row_terms.  ds_ws: device, ws_bytes >= attn_bwd_workspace_bytes;
- * or ds_ws = NULL with ws_bytes = 0, in which case dS is not stored (for
- * callers that take dQ from attn_bwd_queries_fused instead).
+ * attn_row_terms (or attn_bwd_queries_fused).  ds_ws: device, ws_bytes >=
+ * attn_bwd_workspace_bytes; or ds_ws = NULL with ws_bytes = 0, in which case
+ * dS is not stored (for callers that take dQ from attn_bwd_queries_fused).
  */
 ATTN_API int attn_bwd_keys(const attn_shape* shape, const uint16_t* q, const uint16_t* k,
                   const uint16_t* vt, const uint16_t* dout, const float* lse,
@@ -159,21 +159,26 @@ ATTN_API int attn_bwd_queries(const attn_shape* shape, const uint16_t* k,
 
 /*
  * Fused query pass (the query launch streamingAttentionQuerySM86 of
- * StreamingAttentionSM86.alpha, backward-pass header, which walks a query
- * tile's key tiles and forms S, P and dP again): for each 128-query block, S = Q K^T, P = 2^(S c - L),
- * dP = dO V^T and dS = P (dP - D) are recomputed for every visible key block
- * and dQ = s * sum of dS K is accumulated; dS is rounded to binary16 before
- * its product, as in the key pass.  Needs no workspace: pair it with
- * attn_bwd_keys(..., NULL, 0, ...).  It recomputes two products per tile pair
- * to avoid the dS workspace, whose size and traffic grow as T^2 (2 B per
- * visible (query, key) pair and head).  Reads q, k, vt, dout, lse (from
- * attn_fwd) and delta (from attn_row_terms); writes dq for the chunk's
- * query heads.  Device pointers, 16-byte aligned, layouts as above.
+ * StreamingAttentionSM86.alpha, backward-pass header, which forms D for its
+ * rows from dO and the forward's O, writes it for the key launch, and walks
+ * the query tile's key tiles forming S, P and dP again): for each 128-query
+ * block, D = rowsum(dO * O) (stored binary16 O widened, binary32 sum) is
+ * written to delta, then S = Q K^T, P = 2^(S c - L), dP = dO V^T and
+ * dS = P (dP - D) are recomputed for every visible key block and
+ * dQ = s * sum of dS K is accumulated; dS is rounded to binary16 before its
+ * product, as in the key pass.  Needs no workspace and replaces
+ * attn_row_terms: call it after attn_fwd and before
+ * attn_bwd_keys(..., NULL, 0, ...), which reads the delta it wrote.  It
+ * recomputes two products per tile pair to avoid the dS workspace, whose
+ * size and traffic grow as T^2 (2 B per visible (query, key) pair and head).
+ * Reads q, k, vt, dout, o (token-major, from attn_fwd) and lse; writes delta
+ * and dq for the chunk's query heads (rows past a sequence's length: D = 0,
+ * dQ = 0).  Device pointers, 16-byte aligned, layouts as above.
  */
 ATTN_API int attn_bwd_queries_fused(const attn_shape* shape, const uint16_t* q,
                                     const uint16_t* k, const uint16_t* vt,
-                                    const uint16_t* dout, const float* lse,
-                                    const float* delta, float* dq, void* stream);
+                                    const uint16_t* dout, const uint16_t* o, const float* lse,
+                                    float* delta, float* dq, void* stream);
 
 /*
  * Device buffers of one whole problem, as attn_step_host uses them.  All
