@@ -76,6 +76,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attn_bwd_keys.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     lib.attn_bwd_queries.argtypes = [sp, vp, vp, sz, vp, vp]
     lib.attn_bwd_queries_fused.argtypes = [sp] + [vp] * 9
+    lib.attn_bwd_queries_rotated.argtypes = [sp, vp, vp, sz, vp, vp, vp, ctypes.c_int64, vp]
+    lib.attn_bwd_queries_rotated.restype = ctypes.c_int
     lib.attn_bwd_queries_fused.restype = ctypes.c_int
     lib.attn_error_string.argtypes = [ctypes.c_int]
     lib.attn_error_string.restype = ctypes.c_char_p
@@ -241,6 +243,24 @@ def attn_bwd_queries_fused(s: Shape, q, k, vt, dout, o, lse, delta, dq, stream=N
             _want(dq, "dq", torch.float32, (B, H, T, 64)))
     shape = s.c_struct()
     _check("attn_bwd_queries_fused", load_library().attn_bwd_queries_fused(
+        ctypes.byref(shape), *args, _stream_ptr(stream)))
+
+
+def attn_bwd_queries_rotated(s: Shape, k, ws, cos, sin, out, ld=None, stream=None) -> None:
+    """dQ pass with the inverse half-split rotation, bfloat16 token-major
+    ``out`` (row stride ``ld`` elements, default heads * 64)."""
+    B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
+    if not (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.dtype == torch.uint8
+            and ws.is_contiguous()):
+        raise TypeError("ws must be a contiguous uint8 CUDA tensor")
+    if not (isinstance(out, torch.Tensor) and out.is_cuda and out.dtype == torch.bfloat16):
+        raise TypeError("out must be a bfloat16 CUDA tensor")
+    ld = H * 64 if ld is None else int(ld)
+    args = (_want(k, "k", torch.float16, (B, Hkv, T, 64)), ws.data_ptr(), ws.numel(),
+            _want(cos, "cos", torch.float32, (T, 32)), _want(sin, "sin", torch.float32, (T, 32)),
+            out.data_ptr(), ld)
+    shape = s.c_struct()
+    _check("attn_bwd_queries_rotated", load_library().attn_bwd_queries_rotated(
         ctypes.byref(shape), *args, _stream_ptr(stream)))
 
 

@@ -255,6 +255,24 @@ int attn_bwd_queries(const attn_shape* shape, const uint16_t* k, const void* ds_
                             static_cast<cudaStream_t>(stream));
 }
 
+int attn_bwd_queries_rotated(const attn_shape* shape, const uint16_t* k, const void* ds_ws,
+                             size_t ws_bytes, const float* cos_tab, const float* sin_tab,
+                             uint16_t* dq_out, int64_t ld, void* stream) {
+  Dims d;
+  int rc = validate_shape(shape, &d);
+  if (rc != ATTN_OK) return rc;
+  if (!k || !ds_ws || !cos_tab || !sin_tab || !dq_out) return ATTN_ERR_NULL;
+  if (ld < (int64_t)d.H * 64 || ld % 8 != 0) return ATTN_ERR_SHAPE;
+  if (!aligned16(k) || !aligned16(ds_ws) || !aligned16(cos_tab) || !aligned16(sin_tab) ||
+      !aligned16(dq_out))
+    return ATTN_ERR_ALIGN;
+  if (ws_bytes < workspace_bytes_for(d)) return ATTN_ERR_WORKSPACE;
+  DevCtx ctx;
+  if ((rc = device_context(&ctx)) != ATTN_OK) return rc;
+  return launch_bwd_queries(d, ctx, k, static_cast<const uint8_t*>(ds_ws), nullptr,
+                            static_cast<cudaStream_t>(stream), cos_tab, sin_tab, dq_out, ld);
+}
+
 int attn_last_device_error(void* stream) {
   DevCtx ctx;
   int rc = device_context(&ctx);

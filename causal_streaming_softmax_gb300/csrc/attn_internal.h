@@ -72,7 +72,9 @@ int launch_bwd_fused_q(const Dims& d, const DevCtx& ctx, const uint16_t* q, cons
                        const uint16_t* vt, const uint16_t* dout, const uint16_t* o,
                        const float* lse, float* delta, float* dq, cudaStream_t stream);
 int launch_bwd_queries(const Dims& d, const DevCtx& ctx, const uint16_t* k, const uint8_t* ws,
-                       float* dq, cudaStream_t stream);
+                       float* dq, cudaStream_t stream, const float* cos_t = nullptr,
+                       const float* sin_t = nullptr, uint16_t* rot_out = nullptr,
+                       long long ld = 0);
 int launch_wait_probe(const DevCtx& ctx, uint64_t limit_ns, cudaStream_t stream);
 int launch_arith_probe(const float* x, uint32_t* packed, float* e2, int n, cudaStream_t stream);
 

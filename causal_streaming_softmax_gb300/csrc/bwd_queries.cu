@@ -41,6 +41,12 @@ struct QueriesArgs {
   Dims d;
   const uint8_t* ws;
   float* dq;
+  // inverse half-split rotation epilogue (rot_out non-null): cos and sin
+  // tables [T][32], bfloat16 output row p of head h at rot_out[p * ld + 64 h]
+  const float* cos_t;
+  const float* sin_t;
+  uint16_t* rot_out;
+  long long ld;
   uint32_t* err;
   uint64_t wait_ns;
 };
@@ -143,27 +149,56 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ---------------- epilogue: dQ = s * sum ----------------
     const int q = q0 + threadIdx.x;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float* dqrow = a.dq + (((size_t)b * d.H + h) * T + q) * 64;
+    uint32_t r0[32], r1[32];
     if (n_kt > 0) {
       mbar_wait(BAR(BAR_DONE), 0, wc);
       tc_fence_after();
-      uint32_t r0[32], r1[32];
       tmem_ld32x2_wait(tmem + lane_base, tmem + lane_base + 32, r0, r1);
-      if (q < T) {
-        float4* dst = reinterpret_cast<float4*>(dqrow);
+    } else {
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          dst[u] = make_float4(as_f(r0[4 * u]) * d.scale, as_f(r0[4 * u + 1]) * d.scale,
-                               as_f(r0[4 * u + 2]) * d.scale, as_f(r0[4 * u + 3]) * d.scale);
+      for (int u = 0; u < 32; ++u) r0[u] = r1[u] = 0u;  // no visible key: dQ = 0
+    }
+    if (q < T && a.rot_out == nullptr) {
+      float4* dst = reinterpret_cast<float4*>(a.dq + (((size_t)b * d.H + h) * T + q) * 64);
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          dst[8 + u] = make_float4(as_f(r1[4 * u]) * d.scale, as_f(r1[4 * u + 1]) * d.scale,
-                                   as_f(r1[4 * u + 2]) * d.scale, as_f(r1[4 * u + 3]) * d.scale);
-      }
+      for (int u = 0; u < 8; ++u)
+        dst[u] = make_float4(as_f(r0[4 * u]) * d.scale, as_f(r0[4 * u + 1]) * d.scale,
+                             as_f(r0[4 * u + 2]) * d.scale, as_f(r0[4 * u + 3]) * d.scale);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        dst[8 + u] = make_float4(as_f(r1[4 * u]) * d.scale, as_f(r1[4 * u + 1]) * d.scale,
+                                 as_f(r1[4 * u + 2]) * d.scale, as_f(r1[4 * u + 3]) * d.scale);
     } else if (q < T) {
-      float4* dst = reinterpret_cast<float4*>(dqrow);
+      // dQ turned back by the inverse half-split rotation of position q:
+      // column c < 32 pairs with c + 32; out_c = x_c cos + x_{c+32} sin,
+      // out_{c+32} = x_{c+32} cos - x_c sin, each product of the sine
+      // rounded before the fused multiply-add; then packed to bfloat16
+      const float4* cr = reinterpret_cast<const float4*>(a.cos_t + (size_t)q * 32);
+      const float4* sr = reinterpret_cast<const float4*>(a.sin_t + (size_t)q * 32);
+      uint32_t lo[16], hi[16];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) dst[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < 8; ++u) {
+        const float4 cv = __ldg(cr + u), sv = __ldg(sr + u);
+        const float co[4] = {cv.x, cv.y, cv.z, cv.w}, si[4] = {sv.x, sv.y, sv.z, sv.w};
+        float o1[4], o2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x1 = __fmul_rn(as_f(r0[4 * u + e]), d.scale);
+          const float x2 = __fmul_rn(as_f(r1[4 * u + e]), d.scale);
+          o1[e] = fmaf(x1, co[e], __fmul_rn(x2, si[e]));
+          o2[e] = fmaf(x2, co[e], -__fmul_rn(x1, si[e]));
+        }
+        lo[2 * u] = pack_bf16x2(o1[0], o1[1]);
+        lo[2 * u + 1] = pack_bf16x2(o1[2], o1[3]);
+        hi[2 * u] = pack_bf16x2(o2[0], o2[1]);
+        hi[2 * u + 1] = pack_bf16x2(o2[2], o2[3]);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(a.rot_out + ((size_t)b * T + q) * a.ld + 64 * h);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        dst[u] = make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+        dst[4 + u] = make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
+      }
     }
   }
 
@@ -181,7 +216,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 }  // namespace
 
 int launch_bwd_queries(const Dims& d, const DevCtx& ctx, const uint16_t* k, const uint8_t* ws,
-                       float* dq, cudaStream_t stream) {
+                       float* dq, cudaStream_t stream, const float* cos_t, const float* sin_t,
+                       uint16_t* rot_out, long long ld) {
   CUtensorMap tk;
   const uint64_t T = (uint64_t)d.T;
   if (!encode_tmap_3d(&tk, k, 64, T, (uint64_t)d.B * d.Hkv, 128, T * 128, 64, kBN))
@@ -195,7 +231,7 @@ int launch_bwd_queries(const Dims& d, const DevCtx& ctx, const uint16_t* k, cons
                          kSmemBytes);
   });
   if (attr_status[dev & 63] != cudaSuccess) return cuda_status(attr_status[dev & 63]);
-  QueriesArgs args{d, ws, dq, ctx.err, ctx.wait_ns};
+  QueriesArgs args{d, ws, dq, cos_t, sin_t, rot_out, ld, ctx.err, ctx.wait_ns};
   dim3 grid(d.kv_count * d.G, d.nt, d.B);
   bwd_queries_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tk, args);
   return cuda_status(cudaGetLastError());

@@ -230,6 +230,27 @@ ATTN_API int attn_step_host(const attn_shape* shape, const attn_device_buffers* 
                             float* h_dk, float* h_dvt, void* stream);
 
 /*
+ * dQ pass with the inverse half-split rotation in its epilogue (the rotated
+ * form of the dQ-from-scores pass in StreamingAttentionSM86.alpha, the
+ * epilogue that turns dQ back by the inverse rotation and stores the QKV
+ * pullback's bfloat16 operand): as attn_bwd_queries, but each query row
+ * p of head h, x = s * sum, is written as
+ *   out[c]      = x[c] cos[p][c] + x[c + 32] sin[p][c]
+ *   out[c + 32] = x[c + 32] cos[p][c] - x[c] sin[p][c]      (c < 32)
+ * (each sine product rounded to binary32 before the fused multiply-add),
+ * rounded to bfloat16, at dq_out[(b T + p) ld + 64 h + c]: token-major, so
+ * the output can be a column block of a wider [B][T][width] projection
+ * gradient (pass its first column and ld = width).  cos_tab, sin_tab:
+ * device [T][32] binary32.  ld >= heads * 64 and a multiple of 8
+ * (ATTN_ERR_SHAPE otherwise); device pointers, 16-byte aligned.  The
+ * chunk's query heads are written; rows past a sequence's length get 0.
+ */
+ATTN_API int attn_bwd_queries_rotated(const attn_shape* shape, const uint16_t* k,
+                                      const void* ds_ws, size_t ws_bytes, const float* cos_tab,
+                                      const float* sin_tab, uint16_t* dq_out, int64_t ld,
+                                      void* stream);
+
+/*
  * attn_bwd_noalloc - the key pass and the dQ pass (what attn_bwd_keys and
  * then attn_bwd_queries compute) without a caller-supplied workspace.  The
  * method's pages have no counterpart to this entry point.  It is for callers

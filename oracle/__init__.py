@@ -19,7 +19,7 @@ import numpy as np
 from . import build as _build
 
 __all__ = ["forward", "backward", "query_rows", "key_rows", "probs_row",
-           "num_threads", "set_num_threads"]
+           "inverse_rotate", "num_threads", "set_num_threads"]
 
 
 class _Shape(ctypes.Structure):
@@ -162,3 +162,26 @@ def probs_row(q, k, vt, b, h, i, *, causal=True, scale=0.125, lens=None):
     _check(_load().oracle_probs_row(ctypes.byref(s), lp, _ptr(q), _ptr(k), _ptr(vt),
                                     int(b), int(h), int(i), _ptr(p)), "probs_row")
     return p
+
+
+def inverse_rotate(dq, cos, sin):
+    """dQ turned back by the inverse half-split rotation, token-major.
+
+    StreamingAttentionSM86.alpha, the rotated epilogue of the dQ-from-scores
+    pass: for query row p of head h and column c < 32, with (cos, sin) =
+    (cos[p][c], sin[p][c]),
+        out[c]      = dq[c] cos + dq[c + 32] sin
+        out[c + 32] = dq[c + 32] cos - dq[c] sin,
+    stored at row p, columns 64 h + c of a token-major [B][T][H * 64] array.
+    Arguments: dq [B][H][T][64] (already scaled by s), cos and sin [T][32];
+    all widened to binary64 and computed without intermediate rounding.
+    """
+    dq = np.asarray(dq, dtype=np.float64)
+    cos = np.asarray(cos, dtype=np.float64)
+    sin = np.asarray(sin, dtype=np.float64)
+    B, H, T, d = dq.shape
+    half = d // 2
+    x1, x2 = dq[..., :half], dq[..., half:]
+    c, s_ = cos[None, None, :, :half], sin[None, None, :, :half]
+    out = np.concatenate([x1 * c + x2 * s_, x2 * c - x1 * s_], axis=-1)  # [B][H][T][64]
+    return np.ascontiguousarray(out.transpose(0, 2, 1, 3).reshape(B, T, H * d))

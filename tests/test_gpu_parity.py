@@ -328,3 +328,61 @@ def test_fused_dq_head_chunks_match_whole(cuda_device):
     assert api.last_device_error() == 0
     assert np.array_equal(bufs.dq.cpu().numpy(), whole["dq"])
     assert np.array_equal(bufs.delta.cpu().numpy(), whole["delta"])
+
+
+# ---------------------------------------------------------------------------
+# the dQ pass with the inverse half-split rotation (bfloat16, token-major)
+# ---------------------------------------------------------------------------
+def _bf16_rne(x32):
+    b = np.asarray(x32, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint32) << 16
+    return r.astype(np.uint32).view(np.float32)
+
+
+@pytest.mark.parametrize("B,T,H,Hkv,causal,lens", [
+    (1, 512, 8, 2, True, None),
+    (2, 384, 4, 2, False, [100, 384]),
+])
+def test_rotated_dq(cuda_device, B, T, H, Hkv, causal, lens):
+    """attn_bwd_queries_rotated against the oracle's dQ turned back by the
+    inverse rotation, and bit for bit (to one bfloat16 step) against the same
+    epilogue applied on the host to the plain pass's binary32 dQ; written as
+    a column block of a wider token-major buffer whose other columns stay."""
+    import torch
+    from causal_streaming_softmax_gb300 import api
+    inp = workloads.make_custom_inputs(B, T, H, Hkv, causal=causal, lens=lens, seed=T + 3 * H)
+    dev = "cuda"
+    q, k, vt, dout = (torch.from_numpy(inp[n]).to(dev) for n in ("q", "k", "vt", "dout"))
+    ln = None if lens is None else torch.tensor(lens, dtype=torch.int32, device=dev)
+    s = api.Shape(B, T, H, Hkv, causal=causal, seq_lens=ln)
+    bufs = api.Buffers(s)
+    api.forward_backward(s, q, k, vt, dout, bufs)
+    rng = np.random.default_rng(5)
+    theta = rng.uniform(-np.pi, np.pi, size=(T, 32))
+    cos = torch.tensor(np.cos(theta), dtype=torch.float32, device=dev)
+    sin = torch.tensor(np.sin(theta), dtype=torch.float32, device=dev)
+    width, col0 = H * 64 + 3 * 64 + 16, 64 + 8          # a wider projection gradient
+    wide = torch.full((B, T, width), 7.0, dtype=torch.bfloat16, device=dev)
+    api.attn_bwd_queries_rotated(s, k, bufs.ws, cos, sin, wide[:, :, col0:], ld=width)
+    torch.cuda.synchronize()
+    assert api.last_device_error() == 0
+    got = wide.float().cpu().numpy()
+    assert np.all(got[:, :, :col0] == 7.0) and np.all(got[:, :, col0 + H * 64:] == 7.0)
+    got = got[:, :, col0:col0 + H * 64]
+    # against the oracle
+    ref = oracle.backward(inp["q"], inp["k"], inp["vt"], inp["dout"], causal=causal,
+                          scale=0.125, lens=inp["lens"])
+    rot_ref = oracle.inverse_rotate(ref["dq"], cos.cpu().numpy(), sin.cpu().numpy())
+    assert rel_fro(got, rot_ref) <= GRAD_TOL
+    # against the epilogue on the host, from the plain pass's binary32 dQ
+    x = bufs.dq.cpu().numpy().astype(np.float32)              # [B][H][T][64] = s * sum
+    c = cos.cpu().numpy()[None, None].astype(np.float64)
+    sn = sin.cpu().numpy()[None, None].astype(np.float64)
+    x1, x2 = x[..., :32].astype(np.float64), x[..., 32:].astype(np.float64)
+    p2 = (x2 * sn).astype(np.float32).astype(np.float64)
+    p1 = (x1 * sn).astype(np.float32).astype(np.float64)
+    o = np.concatenate([(x1 * c + p2).astype(np.float32), (x2 * c - p1).astype(np.float32)], -1)
+    emu = _bf16_rne(o).transpose(0, 2, 1, 3).reshape(B, T, H * 64)
+    step = np.abs(emu.astype(np.float64)) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(got - emu) <= step)
+    assert np.mean(got == emu) > 0.999

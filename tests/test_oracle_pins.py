@@ -260,3 +260,52 @@ def test_sampled_entry_points_match_full():
                                  lens=lens)
             np.testing.assert_allclose(kr["dk"], full["dk"][b, 1, rows], atol=1e-13)
             np.testing.assert_allclose(kr["dv"], full["dvt"][b, 1][:, rows].T, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# the inverse half-split rotation of the rotated dQ epilogue
+# ---------------------------------------------------------------------------
+def _rope_tables(T, seed):
+    rng = np.random.default_rng(seed)
+    theta = rng.uniform(-np.pi, np.pi, size=(T, 32))
+    return np.cos(theta), np.sin(theta), theta
+
+
+def test_inverse_rotate_identity_and_quarter_turn():
+    """cos = 1, sin = 0 is a pure relayout to token-major; a quarter turn
+    (cos = 0, sin = 1) maps each pair (a, b) to (b, -a)."""
+    rng = np.random.default_rng(3)
+    B, H, T = 2, 3, 5
+    dq = rng.standard_normal((B, H, T, 64))
+    out = oracle.inverse_rotate(dq, np.ones((T, 32)), np.zeros((T, 32)))
+    assert np.array_equal(out.reshape(B, T, H, 64), dq.transpose(0, 2, 1, 3))
+    out = oracle.inverse_rotate(dq, np.zeros((T, 32)), np.ones((T, 32))).reshape(B, T, H, 64)
+    tm = dq.transpose(0, 2, 1, 3)
+    assert np.array_equal(out[..., :32], tm[..., 32:])
+    assert np.array_equal(out[..., 32:], -tm[..., :32])
+
+
+def test_inverse_rotate_is_the_pullback_of_the_forward_rotation():
+    """The epilogue's rotation is the gradient of the forward half-split
+    rotary embedding (each (x_c, x_{c+32}) pair turned by theta_c), taken
+    here by torch autograd on that forward map; it also undoes the forward
+    map and keeps each pair's length."""
+    torch = pytest.importorskip("torch")
+    T = 7
+    cos, sin, theta = _rope_tables(T, 11)
+    rng = np.random.default_rng(12)
+    x = torch.tensor(rng.standard_normal((1, 1, T, 64)), dtype=torch.float64,
+                     requires_grad=True)
+    g = rng.standard_normal((1, 1, T, 64))
+    c = torch.tensor(cos, dtype=torch.float64)
+    s = torch.tensor(sin, dtype=torch.float64)
+    x1, x2 = x[..., :32], x[..., 32:]
+    rot = torch.cat([x1 * c - x2 * s, x2 * c + x1 * s], dim=-1)  # forward rotary map
+    (rot * torch.tensor(g)).sum().backward()
+    pull = oracle.inverse_rotate(g, cos, sin).reshape(1, T, 1, 64).transpose(0, 2, 1, 3)
+    assert np.allclose(pull, x.grad.numpy(), rtol=0, atol=1e-14)
+    back = oracle.inverse_rotate(rot.detach().numpy(), cos, sin).reshape(1, T, 1, 64)
+    assert np.allclose(back.transpose(0, 2, 1, 3), x.detach().numpy(), rtol=0, atol=1e-13)
+    gi = oracle.inverse_rotate(g, cos, sin).reshape(T, 64)
+    g2 = g.reshape(T, 64)
+    assert np.allclose(gi[:, :32] ** 2 + gi[:, 32:] ** 2, g2[:, :32] ** 2 + g2[:, 32:] ** 2)
