@@ -45,6 +45,10 @@ class AttnDeviceBuffers(ctypes.Structure):
                 ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dvt", ctypes.c_void_p)]
 
 
+class AttnProjection(ctypes.Structure):
+    _fields_ = [("f32", ctypes.c_void_p), ("bf16", ctypes.c_void_p), ("ld", ctypes.c_int64)]
+
+
 class AttnError(RuntimeError):
     def __init__(self, fn, code):
         self.code = code
@@ -78,6 +82,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attn_bwd_queries_fused.argtypes = [sp] + [vp] * 9
     lib.attn_bwd_queries_rotated.argtypes = [sp, vp, vp, sz, vp, vp, vp, ctypes.c_int64, vp]
     lib.attn_bwd_queries_rotated.restype = ctypes.c_int
+    pp = ctypes.POINTER(AttnProjection)
+    lib.attn_bwd_keys_projected.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, sz, pp, pp, vp]
+    lib.attn_bwd_keys_projected.restype = ctypes.c_int
+    lib.attn_bwd_queries_projected.argtypes = [sp, vp, vp, sz, pp, vp]
+    lib.attn_bwd_queries_projected.restype = ctypes.c_int
     lib.attn_bwd_queries_fused.restype = ctypes.c_int
     lib.attn_error_string.argtypes = [ctypes.c_int]
     lib.attn_error_string.restype = ctypes.c_char_p
@@ -262,6 +271,43 @@ def attn_bwd_queries_rotated(s: Shape, k, ws, cos, sin, out, ld=None, stream=Non
     shape = s.c_struct()
     _check("attn_bwd_queries_rotated", load_library().attn_bwd_queries_rotated(
         ctypes.byref(shape), *args, _stream_ptr(stream)))
+
+
+def projection(f32=None, bf16=None, ld=None) -> AttnProjection:
+    """A token-major block of a projection gradient: CUDA tensors (views into
+    the wider [B][T][width] gradient, starting at the block's first column),
+    float32 and/or bfloat16, row stride ``ld`` elements."""
+    for t, dt in ((f32, torch.float32), (bf16, torch.bfloat16)):
+        if t is not None and not (t.is_cuda and t.dtype == dt):
+            raise TypeError("projection blocks must be CUDA %s tensors" % dt)
+    if ld is None:
+        raise ValueError("ld (row stride in elements) is required")
+    return AttnProjection(None if f32 is None else f32.data_ptr(),
+                          None if bf16 is None else bf16.data_ptr(), int(ld))
+
+
+def attn_bwd_keys_projected(s: Shape, q, k, vt, dout, lse, delta, ws, dk_out: AttnProjection,
+                            dv_out: AttnProjection, stream=None) -> None:
+    B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
+    args = (_want(q, "q", torch.float16, (B, H, T, 64)),
+            _want(k, "k", torch.float16, (B, Hkv, T, 64)),
+            _want(vt, "vt", torch.float16, (B, Hkv, 64, T)),
+            _want(dout, "dout", torch.float16, (B, H, T, 64)),
+            _want(lse, "lse", torch.float32, (B, H, T)),
+            _want(delta, "delta", torch.float32, (B, H, T)),
+            None if ws is None else ws.data_ptr(), 0 if ws is None else ws.numel())
+    shape = s.c_struct()
+    _check("attn_bwd_keys_projected", load_library().attn_bwd_keys_projected(
+        ctypes.byref(shape), *args, ctypes.byref(dk_out), ctypes.byref(dv_out),
+        _stream_ptr(stream)))
+
+
+def attn_bwd_queries_projected(s: Shape, k, ws, dq_out: AttnProjection, stream=None) -> None:
+    B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
+    shape = s.c_struct()
+    _check("attn_bwd_queries_projected", load_library().attn_bwd_queries_projected(
+        ctypes.byref(shape), _want(k, "k", torch.float16, (B, Hkv, T, 64)), ws.data_ptr(),
+        ws.numel(), ctypes.byref(dq_out), _stream_ptr(stream)))
 
 
 def last_device_error(stream=None) -> int:

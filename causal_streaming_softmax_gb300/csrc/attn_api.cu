@@ -273,6 +273,56 @@ int attn_bwd_queries_rotated(const attn_shape* shape, const uint16_t* k, const v
                             static_cast<cudaStream_t>(stream), cos_tab, sin_tab, dq_out, ld);
 }
 
+namespace {
+// Checks a caller's projection block for `heads` heads of 64 columns.
+int projection_from(const attn_projection* p, int heads, Projection* out) {
+  if (!p || (!p->f32 && !p->bf16)) return ATTN_ERR_NULL;
+  if (p->ld < (int64_t)heads * 64 || p->ld % 8 != 0) return ATTN_ERR_SHAPE;
+  if (!aligned16(p->f32) || !aligned16(p->bf16)) return ATTN_ERR_ALIGN;
+  *out = Projection{p->f32, p->bf16, p->ld};
+  return ATTN_OK;
+}
+}  // namespace
+
+int attn_bwd_keys_projected(const attn_shape* shape, const uint16_t* q, const uint16_t* k,
+                            const uint16_t* vt, const uint16_t* dout, const float* lse,
+                            const float* delta, void* ds_ws, size_t ws_bytes,
+                            const attn_projection* dk_out, const attn_projection* dv_out,
+                            void* stream) {
+  Dims d;
+  int rc = validate_shape(shape, &d);
+  if (rc != ATTN_OK) return rc;
+  const bool store = !(ds_ws == nullptr && ws_bytes == 0);
+  if (!q || !k || !vt || !dout || !lse || !delta || (store && !ds_ws)) return ATTN_ERR_NULL;
+  Projection pk, pv;
+  if ((rc = projection_from(dk_out, d.Hkv, &pk)) != ATTN_OK) return rc;
+  if ((rc = projection_from(dv_out, d.Hkv, &pv)) != ATTN_OK) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(delta) || !aligned16(ds_ws))
+    return ATTN_ERR_ALIGN;
+  if (store && ws_bytes < workspace_bytes_for(d)) return ATTN_ERR_WORKSPACE;
+  DevCtx ctx;
+  if ((rc = device_context(&ctx)) != ATTN_OK) return rc;
+  return launch_bwd_keys(d, ctx, q, k, vt, dout, lse, delta, static_cast<uint8_t*>(ds_ws),
+                         nullptr, nullptr, static_cast<cudaStream_t>(stream), pk, pv);
+}
+
+int attn_bwd_queries_projected(const attn_shape* shape, const uint16_t* k, const void* ds_ws,
+                               size_t ws_bytes, const attn_projection* dq_out, void* stream) {
+  Dims d;
+  int rc = validate_shape(shape, &d);
+  if (rc != ATTN_OK) return rc;
+  if (!k || !ds_ws) return ATTN_ERR_NULL;
+  Projection pq;
+  if ((rc = projection_from(dq_out, d.H, &pq)) != ATTN_OK) return rc;
+  if (!aligned16(k) || !aligned16(ds_ws)) return ATTN_ERR_ALIGN;
+  if (ws_bytes < workspace_bytes_for(d)) return ATTN_ERR_WORKSPACE;
+  DevCtx ctx;
+  if ((rc = device_context(&ctx)) != ATTN_OK) return rc;
+  return launch_bwd_queries(d, ctx, k, static_cast<const uint8_t*>(ds_ws), nullptr,
+                            static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr, 0, pq);
+}
+
 int attn_last_device_error(void* stream) {
   DevCtx ctx;
   int rc = device_context(&ctx);

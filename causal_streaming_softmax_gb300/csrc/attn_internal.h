@@ -34,6 +34,15 @@ struct Dims {
   }
 };
 
+// A token-major block of a projection gradient: element (b, t, head, c) at
+// [(b T + t) ld + 64 head + c]; a null pointer is not written.
+struct Projection {
+  float* f32;
+  uint16_t* bf16;
+  long long ld;
+  __host__ __device__ bool on() const { return f32 != nullptr || bf16 != nullptr; }
+};
+
 struct DevCtx {
   uint32_t* err;     // device error word
   uint64_t wait_ns;  // bounded-wait limit
@@ -67,14 +76,15 @@ int launch_row_terms(const Dims& d, const DevCtx& ctx, const uint16_t* o, const 
 int launch_bwd_keys(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16_t* k,
                     const uint16_t* vt, const uint16_t* dout, const float* lse,
                     const float* delta, uint8_t* ws, float* dk, float* dvt,
-                    cudaStream_t stream);
+                    cudaStream_t stream,
+                    Projection pk = {}, Projection pv = {});
 int launch_bwd_fused_q(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16_t* k,
                        const uint16_t* vt, const uint16_t* dout, const uint16_t* o,
                        const float* lse, float* delta, float* dq, cudaStream_t stream);
 int launch_bwd_queries(const Dims& d, const DevCtx& ctx, const uint16_t* k, const uint8_t* ws,
                        float* dq, cudaStream_t stream, const float* cos_t = nullptr,
                        const float* sin_t = nullptr, uint16_t* rot_out = nullptr,
-                       long long ld = 0);
+                       long long ld = 0, Projection pq = {});
 int launch_wait_probe(const DevCtx& ctx, uint64_t limit_ns, cudaStream_t stream);
 int launch_arith_probe(const float* x, uint32_t* packed, float* e2, int n, cudaStream_t stream);
 

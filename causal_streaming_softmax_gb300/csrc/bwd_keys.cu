@@ -41,6 +41,7 @@
 #include <mutex>
 
 #include "attn_internal.h"
+#include "epilogue.cuh"
 #include "sm103.cuh"
 
 namespace css {
@@ -96,6 +97,7 @@ struct KeysArgs {
   float* dvt;
   uint32_t* err;
   uint64_t wait_ns;
+  Projection pk, pv;  // token-major dK / dV blocks instead of dk, dvt (when on)
 };
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
@@ -442,7 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 32; ++u) r0[u] = r1[u] = 0u;
     }
-    if (store && wg == 0) {
+    if (store && a.pk.on()) {
+      // projection-fused epilogue: row `key` of dK (scaled) or dV, token-major
+      const Projection& pr = wg == 0 ? a.pk : a.pv;
+      store_projection_row(pr, ((size_t)b * T + key) * pr.ld + 64 * (size_t)kv, r0, r1, d.scale,
+                           wg == 0);
+    } else if (store && wg == 0) {
       float4* dst = reinterpret_cast<float4*>(a.dk + (((size_t)b * d.Hkv + kv) * T + key) * 64);
 #pragma unroll
       for (int u = 0; u < 8; ++u)
@@ -478,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 int launch_bwd_keys(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16_t* k,
                     const uint16_t* vt, const uint16_t* dout, const float* lse,
                     const float* delta, uint8_t* ws, float* dk, float* dvt,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, Projection pk, Projection pv) {
   CUtensorMap tq, tk, tv, tdo;
   const uint64_t T = (uint64_t)d.T;
   if (!encode_tmap_3d(&tq, q, 64, T, (uint64_t)d.B * d.H, 128, T * 128, 64, kBQ) ||
@@ -494,7 +501,7 @@ int launch_bwd_keys(const Dims& d, const DevCtx& ctx, const uint16_t* q, const u
     attr_status[dev & 63] = cudaFuncSetAttribute(bwd_keys_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr_status[dev & 63] != cudaSuccess) return cuda_status(attr_status[dev & 63]);
-  KeysArgs args{d, lse, delta, ws, dk, dvt, ctx.err, ctx.wait_ns};
+  KeysArgs args{d, lse, delta, ws, dk, dvt, ctx.err, ctx.wait_ns, pk, pv};
   dim3 grid(d.kv_count, d.nt, d.B);
   bwd_keys_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, args);
   return cuda_status(cudaGetLastError());

@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "attn_internal.h"
+#include "epilogue.cuh"
 #include "sm103.cuh"
 
 namespace css {
@@ -49,6 +50,7 @@ struct QueriesArgs {
   long long ld;
   uint32_t* err;
   uint64_t wait_ns;
+  Projection pq;  // token-major dQ block instead of dq (when on)
 };
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
@@ -60,6 +62,9 @@ static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, ui
   return true;
 }
 
+// EPI: 0 binary32 dQ rows [B][H][T][64]; 1 the inverse half-split rotation
+// to bfloat16 token-major; 2 the projection-fused token-major block.
+template <int EPI>
 __global__ void __launch_bounds__(kThreads, 2)
     bwd_queries_kernel(const __grid_constant__ CUtensorMap tm_k, const QueriesArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -158,7 +163,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int u = 0; u < 32; ++u) r0[u] = r1[u] = 0u;  // no visible key: dQ = 0
     }
-    if (q < T && a.rot_out == nullptr) {
+    if (EPI == 2 && q < T) {
+      // projection-fused epilogue: row q of head h, token-major
+      store_projection_row(a.pq, ((size_t)b * T + q) * a.pq.ld + 64 * (size_t)h, r0, r1, d.scale,
+                           true);
+    } else if (EPI == 0 && q < T) {
       float4* dst = reinterpret_cast<float4*>(a.dq + (((size_t)b * d.H + h) * T + q) * 64);
 #pragma unroll
       for (int u = 0; u < 8; ++u)
@@ -168,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int u = 0; u < 8; ++u)
         dst[8 + u] = make_float4(as_f(r1[4 * u]) * d.scale, as_f(r1[4 * u + 1]) * d.scale,
                                  as_f(r1[4 * u + 2]) * d.scale, as_f(r1[4 * u + 3]) * d.scale);
-    } else if (q < T) {
+    } else if (EPI == 1 && q < T) {
       // dQ turned back by the inverse half-split rotation of position q:
       // column c < 32 pairs with c + 32; out_c = x_c cos + x_{c+32} sin,
       // out_{c+32} = x_{c+32} cos - x_c sin, each product of the sine
@@ -217,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 int launch_bwd_queries(const Dims& d, const DevCtx& ctx, const uint16_t* k, const uint8_t* ws,
                        float* dq, cudaStream_t stream, const float* cos_t, const float* sin_t,
-                       uint16_t* rot_out, long long ld) {
+                       uint16_t* rot_out, long long ld, Projection pq) {
   CUtensorMap tk;
   const uint64_t T = (uint64_t)d.T;
   if (!encode_tmap_3d(&tk, k, 64, T, (uint64_t)d.B * d.Hkv, 128, T * 128, 64, kBN))
@@ -227,13 +236,25 @@ int launch_bwd_queries(const Dims& d, const DevCtx& ctx, const uint16_t* k, cons
   cudaGetDevice(&dev);
   static cudaError_t attr_status[64];
   std::call_once(attr_once[dev & 63], [dev] {
-    attr_status[dev & 63] = cudaFuncSetAttribute(bwd_queries_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(bwd_queries_kernel<0>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bwd_queries_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bwd_queries_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes);
+    attr_status[dev & 63] = e;
   });
   if (attr_status[dev & 63] != cudaSuccess) return cuda_status(attr_status[dev & 63]);
-  QueriesArgs args{d, ws, dq, cos_t, sin_t, rot_out, ld, ctx.err, ctx.wait_ns};
+  QueriesArgs args{d, ws, dq, cos_t, sin_t, rot_out, ld, ctx.err, ctx.wait_ns, pq};
   dim3 grid(d.kv_count * d.G, d.nt, d.B);
-  bwd_queries_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tk, args);
+  if (pq.on())
+    bwd_queries_kernel<2><<<grid, kThreads, kSmemBytes, stream>>>(tk, args);
+  else if (rot_out != nullptr)
+    bwd_queries_kernel<1><<<grid, kThreads, kSmemBytes, stream>>>(tk, args);
+  else
+    bwd_queries_kernel<0><<<grid, kThreads, kSmemBytes, stream>>>(tk, args);
   return cuda_status(cudaGetLastError());
 }
 

@@ -251,6 +251,49 @@ ATTN_API int attn_bwd_queries_rotated(const attn_shape* shape, const uint16_t* k
                                       void* stream);
 
 /*
+ * A token-major block of a fused projection's gradient: the gradient row of
+ * sequence position t and head `head` (64 columns) lives at
+ * [(b T + t) ld + 64 head + c] of f32 (binary32) and of bf16 (bfloat16,
+ * rounded to nearest even from the binary32 value); a NULL pointer is not
+ * written, one of the two must be given.  Point the pointers at the block's
+ * first column inside the wider [B][T][width] gradient and pass ld = width.
+ * ld >= heads * 64 and a multiple of 8 (ATTN_ERR_SHAPE otherwise); both
+ * pointers 16-byte aligned (ATTN_ERR_ALIGN).
+ */
+typedef struct attn_projection {
+  float* f32;
+  uint16_t* bf16;
+  int64_t ld;
+} attn_projection;
+
+/*
+ * Key pass with the projection-fused epilogue (StreamingAttentionSM86.alpha,
+ * the key launch's epilogue that stores dK = s * sum and dV straight into a
+ * fused projection's gradient, token-major, binary32 and bfloat16, instead
+ * of the [head][T][64] dK and [head][64][T] dV^T planes a layout pass then
+ * converted): as attn_bwd_keys, but dK goes to dk_out and dV (row = key
+ * position, not transposed) to dv_out, each with one 64-column block per
+ * K/V head.  ds_ws may be NULL with ws_bytes 0 (no dS store), as there.
+ */
+ATTN_API int attn_bwd_keys_projected(const attn_shape* shape, const uint16_t* q,
+                                     const uint16_t* k, const uint16_t* vt,
+                                     const uint16_t* dout, const float* lse,
+                                     const float* delta, void* ds_ws, size_t ws_bytes,
+                                     const attn_projection* dk_out,
+                                     const attn_projection* dv_out, void* stream);
+
+/*
+ * dQ pass with the projection-fused epilogue (StreamingAttentionSM86.alpha,
+ * the dQ epilogue that stores dQ = s * sum straight into a fused
+ * projection's gradient, token-major, binary32 and bfloat16): as
+ * attn_bwd_queries, but dQ goes to dq_out, one 64-column block per query
+ * head.
+ */
+ATTN_API int attn_bwd_queries_projected(const attn_shape* shape, const uint16_t* k,
+                                        const void* ds_ws, size_t ws_bytes,
+                                        const attn_projection* dq_out, void* stream);
+
+/*
  * attn_bwd_noalloc - the key pass and the dQ pass (what attn_bwd_keys and
  * then attn_bwd_queries compute) without a caller-supplied workspace.  The
  * method's pages have no counterpart to this entry point.  It is for callers

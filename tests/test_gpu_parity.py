@@ -386,3 +386,48 @@ def test_rotated_dq(cuda_device, B, T, H, Hkv, causal, lens):
     step = np.abs(emu.astype(np.float64)) * 2.0 ** -7 + 1e-30
     assert np.all(np.abs(got - emu) <= step)
     assert np.mean(got == emu) > 0.999
+
+
+# ---------------------------------------------------------------------------
+# projection-fused epilogues: dQ, dK, dV written token-major, binary32 + bf16
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("store_ds", [True, False])
+@pytest.mark.parametrize("B,T,H,Hkv,causal,lens", [
+    (1, 384, 8, 2, True, None),
+    (2, 320, 4, 4, False, [100, 320]),
+])
+def test_projection_epilogues(cuda_device, B, T, H, Hkv, causal, lens, store_ds):
+    """The projection blocks hold exactly the plain passes' dQ, dK and dV
+    (dV untransposed) in binary32, their round-to-nearest-even bfloat16, and
+    nothing outside the blocks changes."""
+    import torch
+    from causal_streaming_softmax_gb300 import api
+    inp = workloads.make_custom_inputs(B, T, H, Hkv, causal=causal, lens=lens, seed=T + H)
+    dev = "cuda"
+    q, k, vt, dout = (torch.from_numpy(inp[n]).to(dev) for n in ("q", "k", "vt", "dout"))
+    ln = None if lens is None else torch.tensor(lens, dtype=torch.int32, device=dev)
+    s = api.Shape(B, T, H, Hkv, causal=causal, seq_lens=ln)
+    bufs = api.Buffers(s)
+    api.forward_backward(s, q, k, vt, dout, bufs)
+    # a fused QKV gradient [B][T][width]: Q block, then K, then V, with padding
+    width = (H + 2 * Hkv) * 64 + 32
+    cq, ck, cv = 8, 8 + H * 64, 8 + (H + Hkv) * 64
+    g32 = torch.full((B, T, width), -3.0, dtype=torch.float32, device=dev)
+    g16 = torch.full((B, T, width), -3.0, dtype=torch.bfloat16, device=dev)
+    blk = lambda c0: api.projection(g32[:, :, c0:], g16[:, :, c0:], width)
+    ws = bufs.ws if store_ds else None
+    api.attn_bwd_keys_projected(s, q, k, vt, dout, bufs.lse, bufs.delta, ws, blk(ck), blk(cv))
+    api.attn_bwd_queries_projected(s, k, bufs.ws, blk(cq))
+    torch.cuda.synchronize()
+    assert api.last_device_error() == 0
+    a32 = g32.cpu().numpy()
+    a16 = g16.float().cpu().numpy()
+    want_q = bufs.dq.cpu().numpy().transpose(0, 2, 1, 3).reshape(B, T, H * 64)
+    want_k = bufs.dk.cpu().numpy().transpose(0, 2, 1, 3).reshape(B, T, Hkv * 64)
+    want_v = bufs.dvt.cpu().numpy().transpose(0, 3, 1, 2).reshape(B, T, Hkv * 64)
+    for c0, want in ((cq, want_q), (ck, want_k), (cv, want_v)):
+        n = want.shape[2]
+        assert np.array_equal(a32[:, :, c0:c0 + n], want)
+        assert np.array_equal(a16[:, :, c0:c0 + n], _bf16_rne(want))
+    for arr in (a32, a16):
+        assert np.all(arr[:, :, :cq] == -3.0) and np.all(arr[:, :, cv + Hkv * 64:] == -3.0)
