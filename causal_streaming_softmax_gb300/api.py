@@ -35,7 +35,8 @@ class AttnShape(ctypes.Structure):
                 ("heads", ctypes.c_int32), ("kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("causal", ctypes.c_int32),
                 ("seq_lens", ctypes.c_void_p), ("scale", ctypes.c_float),
-                ("head_begin", ctypes.c_int32), ("head_count", ctypes.c_int32)]
+                ("head_begin", ctypes.c_int32), ("head_count", ctypes.c_int32),
+                ("v_rows", ctypes.c_int32)]
 
 
 class AttnDeviceBuffers(ctypes.Structure):
@@ -130,6 +131,7 @@ class Shape:
     seq_lens: Optional[torch.Tensor] = None
     head_begin: int = 0
     head_count: int = 0
+    v_rows: bool = False  # V as rows [B][Hkv][T][64] instead of V^T [B][Hkv][64][T]
 
     def c_struct(self) -> AttnShape:
         lens = 0
@@ -141,11 +143,17 @@ class Shape:
             lens = t.data_ptr()
         return AttnShape(self.batch, self.seq, self.heads, self.kv_heads, HEAD_DIM,
                          1 if self.causal else 0, lens, float(self.scale),
-                         self.head_begin, self.head_count)
+                         self.head_begin, self.head_count, 1 if self.v_rows else 0)
 
     def chunk(self, head_begin: int, head_count: int) -> "Shape":
         return Shape(self.batch, self.seq, self.heads, self.kv_heads, self.causal, self.scale,
-                     self.seq_lens, head_begin, head_count)
+                     self.seq_lens, head_begin, head_count, self.v_rows)
+
+    def v_shape(self):
+        """Shape of the V argument in this layout."""
+        if self.v_rows:
+            return (self.batch, self.kv_heads, self.seq, HEAD_DIM)
+        return (self.batch, self.kv_heads, HEAD_DIM, self.seq)
 
 
 def _stream_ptr(stream) -> int:
@@ -171,7 +179,7 @@ def attn_fwd(s: Shape, q, k, vt, o, lse, stream=None) -> None:
     B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
     args = (_want(q, "q", torch.float16, (B, H, T, 64)),
             _want(k, "k", torch.float16, (B, Hkv, T, 64)),
-            _want(vt, "vt", torch.float16, (B, Hkv, 64, T)),
+            _want(vt, "vt", torch.float16, s.v_shape()),
             _want(o, "o", torch.float16, (B, T, H * 64)),
             _want(lse, "lse", torch.float32, (B, H, T)))
     shape = s.c_struct()
@@ -215,7 +223,7 @@ def attn_bwd_keys(s: Shape, q, k, vt, dout, lse, delta, ws, dk, dvt, stream=None
         raise TypeError("ws must be a contiguous uint8 CUDA tensor or None")
     args = (_want(q, "q", torch.float16, (B, H, T, 64)),
             _want(k, "k", torch.float16, (B, Hkv, T, 64)),
-            _want(vt, "vt", torch.float16, (B, Hkv, 64, T)),
+            _want(vt, "vt", torch.float16, s.v_shape()),
             _want(dout, "dout", torch.float16, (B, H, T, 64)),
             _want(lse, "lse", torch.float32, (B, H, T)),
             _want(delta, "delta", torch.float32, (B, H, T)),
@@ -244,7 +252,7 @@ def attn_bwd_queries_fused(s: Shape, q, k, vt, dout, o, lse, delta, dq, stream=N
     B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
     args = (_want(q, "q", torch.float16, (B, H, T, 64)),
             _want(k, "k", torch.float16, (B, Hkv, T, 64)),
-            _want(vt, "vt", torch.float16, (B, Hkv, 64, T)),
+            _want(vt, "vt", torch.float16, s.v_shape()),
             _want(dout, "dout", torch.float16, (B, H, T, 64)),
             _want(o, "o", torch.float16, (B, T, H * 64)),
             _want(lse, "lse", torch.float32, (B, H, T)),
@@ -291,7 +299,7 @@ def attn_bwd_keys_projected(s: Shape, q, k, vt, dout, lse, delta, ws, dk_out: At
     B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
     args = (_want(q, "q", torch.float16, (B, H, T, 64)),
             _want(k, "k", torch.float16, (B, Hkv, T, 64)),
-            _want(vt, "vt", torch.float16, (B, Hkv, 64, T)),
+            _want(vt, "vt", torch.float16, s.v_shape()),
             _want(dout, "dout", torch.float16, (B, H, T, 64)),
             _want(lse, "lse", torch.float32, (B, H, T)),
             _want(delta, "delta", torch.float32, (B, H, T)),
@@ -402,7 +410,7 @@ class DeviceInputs:
         B, T, H, Hkv = s.batch, s.seq, s.heads, s.kv_heads
         self.q = torch.empty((B, H, T, 64), dtype=torch.float16, device=dev)
         self.k = torch.empty((B, Hkv, T, 64), dtype=torch.float16, device=dev)
-        self.vt = torch.empty((B, Hkv, 64, T), dtype=torch.float16, device=dev)
+        self.vt = torch.empty(s.v_shape(), dtype=torch.float16, device=dev)
         self.dout = torch.empty((B, H, T, 64), dtype=torch.float16, device=dev)
 
 

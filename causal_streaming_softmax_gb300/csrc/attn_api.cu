@@ -88,6 +88,7 @@ int validate_shape(const attn_shape* s, Dims* d) {
   if (s->heads % s->kv_heads != 0) return ATTN_ERR_SHAPE;
   if (s->head_dim != 64) return ATTN_ERR_SHAPE;
   if (s->causal != 0 && s->causal != 1) return ATTN_ERR_SHAPE;
+  if (s->v_rows != 0 && s->v_rows != 1) return ATTN_ERR_SHAPE;
   if (!(s->scale > 0.0f) || !isfinite(s->scale)) return ATTN_ERR_SHAPE;
   int begin = s->head_begin, count = s->head_count;
   if (begin < 0 || count < 0) return ATTN_ERR_SHAPE;
@@ -109,6 +110,7 @@ int validate_shape(const attn_shape* s, Dims* d) {
   d->kv_count = count;
   d->nt = (s->seq + kTile - 1) / kTile;
   d->npairs = s->causal ? (long long)d->nt * (d->nt + 1) / 2 : (long long)d->nt * d->nt;
+  d->v_rows = s->v_rows;
   d->ws_heads = 0;
   d->ws_h0 = 0;
   return ATTN_OK;

@@ -26,6 +26,7 @@ struct Dims {
   int kv_count;
   int nt;               // ceil(T / 128)
   long long npairs;     // workspace tiles per query head
+  int v_rows;           // V given as rows [B][Hkv][T][64] (else V^T [B][Hkv][64][T])
   int ws_heads;         // query heads per batch in the workspace layout (0: kv_count * G)
   int ws_h0;            // layout index of the chunk's first query head
   // workspace tile index of (query tile i, key tile j)

@@ -60,6 +60,7 @@ constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);   // Q (tmem) x K (K-major)
 constexpr uint32_t kIdescDP = idesc_f16_f32(128, 128, 0, 1);  // dO (tmem) x V (MN-major, from V^T)
+constexpr uint32_t kIdescDPR = idesc_f16_f32(128, 128, 0, 0); // dO (tmem) x V rows (K-major)
 constexpr uint32_t kIdescDQ = idesc_f16_f32(128, 64, 0, 1);   // dS (tmem) x K (MN-major)
 
 enum {
@@ -194,8 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
         mbar_arrive_expect_tx(BAR(BAR_KV_FULL + s), kStageBytes);
         tma_load_3d(st + kStK, &tm_k, BAR(BAR_KV_FULL + s), 0, j * kBN, kvplane);
-        tma_load_3d(st + kStVT, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN, 0, kvplane);
-        tma_load_3d(st + kStVT + 8192, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN + 64, 0, kvplane);
+        if (d.v_rows) {
+          tma_load_3d(st + kStVT, &tm_vt, BAR(BAR_KV_FULL + s), 0, j * kBN, kvplane);  // as K
+        } else {
+          tma_load_3d(st + kStVT, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN, 0, kvplane);
+          tma_load_3d(st + kStVT + 8192, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN + 64, 0, kvplane);
+        }
         issued = j + 1;
       }
       drain_wait(BAR(BAR_QD_FULL), 0, a.wait_ns);
@@ -223,10 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // halves 8 KiB apart
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bdesc = role == 0
-                                       ? sdesc_sw128(st + kStK + kk * 32, 16, 1024)
-                                       : sdesc_sw128(st + kStVT + kk * 2048, 8192, 1024);
-            mma_ts(dcol, tmem + a_col + kk * 8, bdesc, role == 0 ? kIdescS : kIdescDP, kk > 0);
+            // V given as rows is K-major like K
+            const uint64_t bdesc =
+                role == 0   ? sdesc_sw128(st + kStK + kk * 32, 16, 1024)
+                : d.v_rows ? sdesc_sw128(st + kStVT + kk * 32, 16, 1024)
+                           : sdesc_sw128(st + kStVT + kk * 2048, 8192, 1024);
+            const uint32_t idesc = role == 0 ? kIdescS : (d.v_rows ? kIdescDPR : kIdescDP);
+            mma_ts(dcol, tmem + a_col + kk * 8, bdesc, idesc, kk > 0);
           }
           mma_commit(BAR(BAR_S_FULL));
         }
@@ -394,7 +402,8 @@ int launch_bwd_fused_q(const Dims& d, const DevCtx& ctx, const uint16_t* q, cons
   if (!encode_tmap_3d(&tq, q, 64, T, (uint64_t)d.B * d.H, 128, T * 128, 64, kBM) ||
       !encode_tmap_3d(&tdo, dout, 64, T, (uint64_t)d.B * d.H, 128, T * 128, 64, kBM) ||
       !encode_tmap_3d(&tk, k, 64, T, (uint64_t)d.B * d.Hkv, 128, T * 128, 64, kBN) ||
-      !encode_tmap_3d(&tv, vt, T, 64, (uint64_t)d.B * d.Hkv, T * 2, T * 128, 64, 64))
+      !(d.v_rows ? encode_tmap_3d(&tv, vt, 64, T, (uint64_t)d.B * d.Hkv, 128, T * 128, 64, 128)
+                  : encode_tmap_3d(&tv, vt, T, 64, (uint64_t)d.B * d.Hkv, T * 2, T * 128, 64, 64)))
     return ATTN_ERR_CUDA;
   static std::once_flag attr_once[64];
   int dev = 0;

@@ -229,8 +229,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kvplane = b * d.Hkv + kv;
       mbar_arrive_expect_tx(BAR(BAR_KV_FULL), 32768);
       tma_load_3d(sbase + kSmemK, &tm_k, BAR(BAR_KV_FULL), 0, k0, kvplane);
-      tma_load_3d(sbase + kSmemV, &tm_vt, BAR(BAR_KV_FULL), k0, 0, kvplane);
-      tma_load_3d(sbase + kSmemV + 8192, &tm_vt, BAR(BAR_KV_FULL), k0 + 64, 0, kvplane);
+      if (d.v_rows) {
+        tma_load_3d(sbase + kSmemV, &tm_vt, BAR(BAR_KV_FULL), 0, k0, kvplane);  // V rows, as K
+      } else {
+        tma_load_3d(sbase + kSmemV, &tm_vt, BAR(BAR_KV_FULL), k0, 0, kvplane);
+        tma_load_3d(sbase + kSmemV + 8192, &tm_vt, BAR(BAR_KV_FULL), k0 + 64, 0, kvplane);
+      }
       int issued = 0, g = 0, rem = 0;
       for (int n = 0; n < n_steps; ++n) {
         const int s = n % kStages;
@@ -339,10 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // K (warps 0-3) or V (warps 4-7) row r into tensor memory as A operands
       ok = mbar_wait_warp(BAR(BAR_KV_FULL), 0, wc);
       uint32_t w[32];
-      if (wg == 0) {
+      if (wg == 0 || d.v_rows) {
+        // K, or V given as rows: row r of the tile, eight 16-byte chunks
+        const uint8_t* tile = sgen + (wg == 0 ? kSmemK : kSmemV);
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
-          const uint4 v = *reinterpret_cast<const uint4*>(sgen + kSmemK + sw128_offset(r, ch));
+          const uint4 v = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, ch));
           w[4 * ch] = v.x, w[4 * ch + 1] = v.y, w[4 * ch + 2] = v.z, w[4 * ch + 3] = v.w;
         }
       } else {
@@ -491,7 +497,8 @@ int launch_bwd_keys(const Dims& d, const DevCtx& ctx, const uint16_t* q, const u
   if (!encode_tmap_3d(&tq, q, 64, T, (uint64_t)d.B * d.H, 128, T * 128, 64, kBQ) ||
       !encode_tmap_3d(&tdo, dout, 64, T, (uint64_t)d.B * d.H, 128, T * 128, 64, kBQ) ||
       !encode_tmap_3d(&tk, k, 64, T, (uint64_t)d.B * d.Hkv, 128, T * 128, 64, kBK) ||
-      !encode_tmap_3d(&tv, vt, T, 64, (uint64_t)d.B * d.Hkv, T * 2, T * 128, 64, 64))
+      !(d.v_rows ? encode_tmap_3d(&tv, vt, 64, T, (uint64_t)d.B * d.Hkv, 128, T * 128, 64, 128)
+                  : encode_tmap_3d(&tv, vt, T, 64, (uint64_t)d.B * d.Hkv, T * 2, T * 128, 64, 64)))
     return ATTN_ERR_CUDA;
   static std::once_flag attr_once[64];
   int dev = 0;

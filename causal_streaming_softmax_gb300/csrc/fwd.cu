@@ -50,6 +50,7 @@ constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);  // Q (K-major) x K (K-major)
 constexpr uint32_t kIdescO = idesc_f16_f32(128, 64, 0, 0);   // P (tmem) x V^T (K-major)
+constexpr uint32_t kIdescOR = idesc_f16_f32(128, 64, 0, 1);  // P (tmem) x V rows (MN-major)
 
 enum {
   BAR_Q = 0,
@@ -65,7 +66,7 @@ enum {
 static_assert(BAR_COUNT * 8 <= 256, "barrier area");
 
 struct FwdArgs {
-  int T, H, Hkv, G, causal;
+  int T, H, Hkv, G, causal, v_rows;
   const int32_t* lens;
   float c;
   uint16_t* o;
@@ -184,6 +185,9 @@ __device__ __forceinline__ void store_p(uint32_t t_p, const uint32_t (&pk)[64]) 
 }
 
 // 12 warps: three per scheduler, so up to 168 registers per thread.
+// VROWS: V given as rows [B][Hkv][T][64] (else V^T), fixed at compile time
+// so that each layout's kernel carries only its own addressing.
+template <bool VROWS>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_vt, const FwdArgs a) {
@@ -255,9 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = sbase + kSmemStage0 + s * kStageBytes;
         mbar_arrive_expect_tx(BAR(BAR_KV_FULL + s), kStageBytes);
         tma_load_3d(st, &tm_k, BAR(BAR_KV_FULL + s), 0, j * kBN, kvplane);
-        tma_load_3d(st + kTileBytes, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN, 0, kvplane);
-        tma_load_3d(st + kTileBytes + 8192, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN + 64, 0,
-                    kvplane);
+        if (VROWS) {
+          tma_load_3d(st + kTileBytes, &tm_vt, BAR(BAR_KV_FULL + s), 0, j * kBN, kvplane);
+        } else {
+          tma_load_3d(st + kTileBytes, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN, 0, kvplane);
+          tma_load_3d(st + kTileBytes + 8192, &tm_vt, BAR(BAR_KV_FULL + s), j * kBN + 64, 0,
+                      kvplane);
+        }
         issued = j + 1;
       }
       // no copy may still be landing when the CTA exits (matters only when a
@@ -314,7 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
               mma_ts(tmem + kColO + 64 * t, tmem + kColP + 64 * t + kk * 8,
-                     sdesc_sw128(v_s + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), kIdescO,
+                     VROWS ? sdesc_sw128(v_s + kk * 2048, 8192, 1024)
+                              : sdesc_sw128(v_s + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                     VROWS ? kIdescOR : kIdescO,
                      (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit(BAR(BAR_P_FREE + t));
           }
@@ -457,20 +467,29 @@ int launch_fwd(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16
   // Q [B*H][T][64], K [B*Hkv][T][64]: boxes of 128 rows x 64 values.
   if (!encode_tmap_3d(&tq, q, 64, T, (uint64_t)d.B * d.H, 128, T * 128, 64, kBM) ||
       !encode_tmap_3d(&tk, k, 64, T, (uint64_t)d.B * d.Hkv, 128, T * 128, 64, kBN) ||
-      // V^T [B*Hkv][64][T]: boxes of 64 keys x 64 rows.
-      !encode_tmap_3d(&tv, vt, T, 64, (uint64_t)d.B * d.Hkv, T * 2, T * 128, 64, 64))
+      // V^T [B*Hkv][64][T]: boxes of 64 keys x 64 rows; V rows: 128 keys x 64
+      !(d.v_rows ? encode_tmap_3d(&tv, vt, 64, T, (uint64_t)d.B * d.Hkv, 128, T * 128, 64, 128)
+                  : encode_tmap_3d(&tv, vt, T, 64, (uint64_t)d.B * d.Hkv, T * 2, T * 128, 64, 64)))
     return ATTN_ERR_CUDA;
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaGetDevice(&dev);
   static cudaError_t attr_status[64];
   std::call_once(attr_once[dev & 63], [dev] {
-    attr_status[dev & 63] = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes);
+    attr_status[dev & 63] = e;
   });
   if (attr_status[dev & 63] != cudaSuccess) return cuda_status(attr_status[dev & 63]);
-  FwdArgs args{d.T, d.H, d.Hkv, d.G, d.causal, d.lens, d.c, o, lse, ctx.err, ctx.wait_ns};
+  FwdArgs args{d.T, d.H, d.Hkv, d.G, d.causal, d.v_rows, d.lens, d.c, o, lse, ctx.err, ctx.wait_ns};
   dim3 grid(d.H, (d.T + 2 * kBM - 1) / (2 * kBM), d.B);
-  fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, args);
+  if (d.v_rows)
+    fwd_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, args);
+  else
+    fwd_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, args);
   return cuda_status(cudaGetLastError());
 }
 

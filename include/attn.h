@@ -91,6 +91,11 @@ enum {
  *   workspace holds the chunk only, so a caller can bound it (or keep it
  *   L2-resident) by walking the heads in chunks.  attn_fwd and
  *   attn_row_terms ignore the chunk.
+ * v_rows: 0: every `vt` argument is V^T, [B][Hkv][64][T] (the pages' forward
+ *   layout); 1: it is V as rows, [B][Hkv][T][64] (K's layout, the pages'
+ *   backward layout and their row-V forward), so no transposed copy of V
+ *   is needed.  Results are the same either way.  Other values:
+ *   ATTN_ERR_SHAPE.
  */
 typedef struct attn_shape {
   int32_t batch;
@@ -103,6 +108,7 @@ typedef struct attn_shape {
   float scale;
   int32_t head_begin;
   int32_t head_count;
+  int32_t v_rows;
 } attn_shape;
 
 /*

@@ -431,3 +431,33 @@ def test_projection_epilogues(cuda_device, B, T, H, Hkv, causal, lens, store_ds)
         assert np.array_equal(a16[:, :, c0:c0 + n], _bf16_rne(want))
     for arr in (a32, a16):
         assert np.all(arr[:, :, :cq] == -3.0) and np.all(arr[:, :, cv + Hkv * 64:] == -3.0)
+
+
+# ---------------------------------------------------------------------------
+# V given as rows [B][Hkv][T][64] instead of V^T
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("B,T,H,Hkv,causal,lens", [
+    (1, 512, 8, 2, True, None),
+    (2, 320, 4, 4, False, [100, 320]),
+])
+def test_v_rows_layout(cuda_device, B, T, H, Hkv, causal, lens, fused):
+    """The whole path with V as rows gives the same bits as with V^T (the
+    operands are the same values read through another descriptor), and
+    matches the oracle."""
+    import torch
+    from causal_streaming_softmax_gb300 import api
+    inp = workloads.make_custom_inputs(B, T, H, Hkv, causal=causal, lens=lens, seed=T + 9)
+    ref = run_gpu(inp, causal=causal, fused_dq=fused)
+    dev = "cuda"
+    q, k, dout = (torch.from_numpy(inp[n]).to(dev) for n in ("q", "k", "dout"))
+    v = torch.from_numpy(np.ascontiguousarray(inp["vt"].transpose(0, 1, 3, 2))).to(dev)
+    ln = None if lens is None else torch.tensor(lens, dtype=torch.int32, device=dev)
+    s = api.Shape(B, T, H, Hkv, causal=causal, seq_lens=ln, v_rows=True)
+    bufs = api.Buffers(s, workspace=not fused)
+    api.forward_backward(s, q, k, v, dout, bufs, fused_dq=fused)
+    torch.cuda.synchronize()
+    assert api.last_device_error() == 0
+    for name in ("o", "lse", "delta", "dq", "dk", "dvt"):
+        assert np.array_equal(getattr(bufs, name).cpu().numpy(), ref[name], equal_nan=True), name
+    compare_full(ref, _full(inp, causal), inp)
