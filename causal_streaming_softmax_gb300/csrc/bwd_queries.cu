@@ -5,7 +5,11 @@
 // Method (StreamingAttentionSM86.alpha, streamingAttentionQueryFromScores
 // section and the page-1 header of the split backward): for each key tile up
 // to the diagonal, dQ += dS K with dS taken from the stored dS^T read
-// transposed; the epilogue scales by s and stores binary32 rows.
+// transposed; the epilogue scales by s and stores binary32 rows, or (the
+// pages' other epilogues) turns dQ back by the inverse half-split rotation
+// into bfloat16 token-major rows, or writes a token-major block of a fused
+// projection gradient in binary32 and bfloat16 (a template parameter picks
+// one, so each variant carries only its own code).
 //
 // GB300 design: warp 4 copies each workspace tile (32 KiB, already in the
 // shared-memory image the tensor core reads) with one bulk copy and K's tile

@@ -13,11 +13,12 @@
 // tile and ping-pong on the exponential unit:
 //   warps 0-3   softmax of tile A, one thread per query row (= TMEM lane)
 //   warps 4-7   softmax of tile B
-//   warp 8      TMA producer: Q once, then K / V^T tiles through a 3-stage ring
+//   warp 8      TMA producer: Q once, then K and V^T (or V rows) tiles
+//               through a 3-stage ring
 //   warps 9-11  MMA issuers: S_A = Q_A K^T and S_B = Q_B K^T (warp 9),
-//               O_A += P_A V (warp 10), O_B += P_B V (warp 11).  A
-//               tcgen05.mma blocks its issuing thread longer than the tensor
-//               core takes for it, so independent chains get their own warps.
+//               O_A += P_A V (warp 10), O_B += P_B V (warp 11): independent
+//               chains get their own warps, so one chain waiting on its
+//               barrier never holds back another's issue.
 // Tensor memory (512 columns): S_A 0-127, S_B 128-255 (binary32), P_A
 // 256-319, P_B 320-383 (binary16 pairs), O_A 384-447, O_B 448-511.  Since P
 // has its own columns, S of the next key tile is computed as soon as the
