@@ -21,7 +21,8 @@ timed region, the copies overlapped with the kernels),
 ``cpu_baseline`` the binary64 oracle on a bounded sample timed on the host,
 and ``fused_dq_variant`` the same step as the pages' two-launch backward:
 the fused query pass (D and dQ, recomputing S, P, dP) then the key pass
-storing no dS (no workspace), timed separately.
+storing no dS (no workspace), timed separately, with its own host-to-host
+``e2e`` (attn_step_host without a workspace).
 
 ``--impl reference`` times the oracle (the CPU reference of this method) on
 the same workload, one bounded sample per step, and prints the same line
@@ -363,12 +364,12 @@ def run_ours(args, w, world, rank, local):
         kernels[n] = e
 
     # ---- end to end through the host-buffer API ----
-    e2e = None
-    if not args.no_e2e:
-        host = api.HostProblem(s, *(torch.from_numpy(inp[n]) for n in ("q", "k", "vt", "dout")))
-        dev_in = api.DeviceInputs(s, dev)
+    host = dev_in = None
+
+    def time_e2e(step_bufs):
+        # K host-to-host steps through attn_step_host, copies inside the events
         for _ in range(max(1, min(args.warmup, 3))):
-            api.forward_backward_host(s, host, dev_in, bufs, stream)
+            api.forward_backward_host(s, host, dev_in, step_bufs, stream)
         torch.cuda.synchronize(dev)
         Ke = max(1, min(K, 50))
         e0 = torch.cuda.Event(enable_timing=True)
@@ -377,16 +378,22 @@ def run_ours(args, w, world, rank, local):
         torch.cuda.synchronize(dev)
         e0.record(stream)
         for _ in range(Ke):
-            api.forward_backward_host(s, host, dev_in, bufs, stream)
+            api.forward_backward_host(s, host, dev_in, step_bufs, stream)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         dist_barrier(world)
         e_ms = dist_max(e0.elapsed_time(e1), world)
         if api.last_device_error(stream) != 0:
             raise RuntimeError("device error during the end-to-end steps")
-        e2e = dict(value=world * fl["step"] * Ke / (e_ms / 1e3) / 1e12, unit="TFLOP/s",
-                   h2d_bytes_per_step=host.input_bytes(), d2h_bytes_per_step=host.output_bytes(),
-                   steps=Ke, ms_per_step=e_ms / Ke)
+        return dict(value=world * fl["step"] * Ke / (e_ms / 1e3) / 1e12, unit="TFLOP/s",
+                    h2d_bytes_per_step=host.input_bytes(), d2h_bytes_per_step=host.output_bytes(),
+                    steps=Ke, ms_per_step=e_ms / Ke)
+
+    e2e = None
+    if not args.no_e2e:
+        host = api.HostProblem(s, *(torch.from_numpy(inp[n]) for n in ("q", "k", "vt", "dout")))
+        dev_in = api.DeviceInputs(s, dev)
+        e2e = time_e2e(bufs)
 
     # ---- the same step with the fused query pass (no dS workspace) ----
     variant = None
@@ -426,6 +433,9 @@ def run_ours(args, w, world, rank, local):
             ms_per_step=f_ms / Kf,
             kernels_ms={n: sum(fev[i][c].elapsed_time(fev[i][c + 1]) for i in range(Kf)) / Kf
                         for c, (n, _) in enumerate(fcalls)})
+        if host is not None:
+            # the same host-to-host step on this path (attn_step_host without a workspace)
+            variant["e2e"] = time_e2e(fbufs)
         del fbufs
 
     cpu = None

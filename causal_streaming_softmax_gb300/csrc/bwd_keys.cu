@@ -109,47 +109,38 @@ static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, ui
   return true;
 }
 
-// Probabilities of 32 queries for one key row: P = 2^(S c - L), kept in
-// binary32 for dS and packed to binary16 pairs for dV.  MASK zeroes the
-// entries outside [qlo, qhi) (local query indices).
+// One key row's step for 32 queries: P = 2^(S c - L) and dS = P (dP - D),
+// both packed to binary16 pairs (P for dV, dS for dK and the workspace); dS
+// takes P unrounded.  MASK zeroes P, so also dS, outside [qlo, qhi) (local
+// query indices).  Both formulas sit in one basic block, so the compiler can
+// interleave one pair's exponentials with another pair's score-gradient
+// arithmetic (separate blocks cost 5% of the kernel); dP - D is one FFMA2
+// with factor -1, which rounds exactly as the subtraction.
 template <bool MASK>
-__device__ __forceinline__ void probabilities(const uint32_t (&sv)[32],
-                                              const float4* __restrict__ L4, float c, int qlo,
-                                              int qhi, float2 (&p)[16], uint32_t (&pp)[16]) {
+__device__ __forceinline__ void step_math(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
+                                          const float4* __restrict__ L4,
+                                          const float4* __restrict__ D4, float c, int qlo,
+                                          int qhi, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
   const float2 c2 = make_float2(c, c);
+  const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
     const float4 l = L4[u];
+    const float4 dl = D4[u];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int e = 4 * u + 2 * h;
       const float2 nl = h ? make_float2(-l.z, -l.w) : make_float2(-l.x, -l.y);
+      const float2 d2 = h ? make_float2(dl.z, dl.w) : make_float2(dl.x, dl.y);
       const float2 t = __ffma2_rn(make_float2(as_f(sv[e]), as_f(sv[e + 1])), c2, nl);
       float2 q = make_float2(ex2_approx(t.x), ex2_approx(t.y));
       if (MASK) {
         if (e < qlo || e >= qhi) q.x = 0.f;
         if (e + 1 < qlo || e + 1 >= qhi) q.y = 0.f;
       }
-      p[e >> 1] = q;
       pp[e >> 1] = pack_f16x2(q.x, q.y);
-    }
-  }
-}
-
-// Score gradients dS = P (dP - D) of the same 32 queries, packed to binary16
-// pairs (a masked P is zero, so is its dS).
-__device__ __forceinline__ void score_gradients(const float2 (&p)[16], const uint32_t (&dv)[32],
-                                                const float4* __restrict__ D4,
-                                                uint32_t (&dd)[16]) {
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const float4 dl = D4[u];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int e = 4 * u + 2 * h;
-      const float2 nd = h ? make_float2(-dl.z, -dl.w) : make_float2(-dl.x, -dl.y);
-      const float2 g = __fadd2_rn(make_float2(as_f(dv[e]), as_f(dv[e + 1])), nd);
-      const float2 ds = __fmul2_rn(p[e >> 1], g);
+      const float2 g = __ffma2_rn(d2, m1, make_float2(as_f(dv[e]), as_f(dv[e + 1])));
+      const float2 ds = __fmul2_rn(q, g);
       dd[e >> 1] = pack_f16x2(ds.x, ds.y);
     }
   }
@@ -398,13 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           (d.causal && qb < k0 + kBK - 1) || (qb + 32 > len) || (k0 + kBK > len);
       const int qlo = (d.causal ? key : 0) - qb;
       const int qhi = (key < len ? len : 0) - qb;
-      float2 p[16];
       uint32_t pp[16], dd[16];
       if (need_mask)
-        probabilities<true>(sv, L4, c, qlo, qhi, p, pp);
+        step_math<true>(sv, dv, L4, D4, c, qlo, qhi, pp, dd);
       else
-        probabilities<false>(sv, L4, c, qlo, qhi, p, pp);
-      score_gradients(p, dv, D4, dd);
+        step_math<false>(sv, dv, L4, D4, c, qlo, qhi, pp, dd);
       // pair buffer pb was last read by dV and dK of step n-2
       if (n >= 2 && !mbar_wait_warp(BAR(BAR_PK_FREE + pb), ((n >> 1) - 1) & 1, wc)) {
         ok = false;
