@@ -42,6 +42,9 @@ EDGE = [
     # the forward's K/V stage ring holds
     (2, 1024, 2, 2, False, [600, 1000]),
     (1, 1024, 4, 1, True, [600]),
+    # empty sequences in a batch: no row and no key of theirs is valid
+    (3, 256, 4, 2, True, [0, 100, 256]),
+    (2, 128, 2, 1, False, [0, 128]),
 ]
 
 
@@ -248,6 +251,7 @@ FUSED = [
     (3, 384, 4, 2, True, [1, 129, 384]),
     (2, 1024, 2, 2, False, [600, 1000]),
     (1, 1024, 8, 8, True, None),
+    (3, 256, 4, 2, True, [0, 100, 256]),  # an empty sequence
 ]
 
 
