@@ -147,6 +147,9 @@ __device__ __forceinline__ void step_math(const uint32_t (&sv)[32], const uint32
 }
 
 // 14 warps put four on a scheduler, which caps a thread at 128 registers.
+// STORE: dS^T is kept in the workspace (fixed per launch, so the step loop
+// carries only its own waits).
+template <bool STORE>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_keys_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 13) {
     // ---------------- store: dS^T of each step into the workspace ----------------
     // (no workspace: dS is not kept, for a dQ pass that recomputes it)
-    if (lane == 0 && n_steps > 0 && a.ws != nullptr) {
+    if (STORE && lane == 0 && n_steps > 0) {
       const int Hc = d.ws_heads ? d.ws_heads : d.kv_count * d.G;
       const int h_local0 = d.ws_h0 + (kv - d.kv_begin) * d.G;
       int g = 0, rem = 0;
@@ -328,7 +331,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = k0 + r;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float c = d.c;
-    const bool store_ds = a.ws != nullptr;
     bool ok = true;
     if (n_steps > 0) {
       // K (warps 0-3) or V (warps 4-7) row r into tensor memory as A operands
@@ -394,24 +396,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         step_math<true>(sv, dv, L4, D4, c, qlo, qhi, pp, dd);
       else
         step_math<false>(sv, dv, L4, D4, c, qlo, qhi, pp, dd);
-      // pair buffer pb was last read by dV and dK of step n-2
-      if (n >= 2 && !mbar_wait_warp(BAR(BAR_PK_FREE + pb), ((n >> 1) - 1) & 1, wc)) {
-        ok = false;
-        break;
+      // pair buffer pb was last read by dV and dK of step n-2; with the
+      // store, shared dS^T buffer n % 3 was last filled at step n-3 and its
+      // bulk store must have read it.  Both are almost always free: one vote
+      // covers both checks, and the bounded waits run only when one is not.
+      const int dsbuf = n % kDSBufs;
+      if (!STORE) {
+        if (n >= 2 && !mbar_wait_warp(BAR(BAR_PK_FREE + pb), ((n >> 1) - 1) & 1, wc)) {
+          ok = false;
+          break;
+        }
+      } else {
+        const bool f1 = n < 2 || mbar_try_wait(BAR(BAR_PK_FREE + pb), ((n >> 1) - 1) & 1);
+        const bool f2 =
+            n < kDSBufs || mbar_try_wait(BAR(BAR_DS_STORED + dsbuf), ((n / kDSBufs) - 1) & 1);
+        if (!__all_sync(0xffffffffu, f1 && f2)) {
+          if (n >= 2 && !mbar_wait_warp(BAR(BAR_PK_FREE + pb), ((n >> 1) - 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          if (n >= kDSBufs &&
+              !mbar_wait_warp(BAR(BAR_DS_STORED + dsbuf), ((n / kDSBufs) - 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+        }
       }
       tc_fence_after();
       const uint32_t pk = kColPK + 64 * pb + 16 * wg;
       tmem_st16(tmem + lane_base + pk, pp);
       tmem_st16(tmem + lane_base + pk + 32, dd);
 
-      if (store_ds) {
-        // shared dS^T buffer n % 3 was last filled at step n-3: its bulk store has read it
-        const int dsbuf = n % kDSBufs;
-        if (n >= kDSBufs &&
-            !mbar_wait_warp(BAR(BAR_DS_STORED + dsbuf), ((n / kDSBufs) - 1) & 1, wc)) {
-          ok = false;
-          break;
-        }
+      if (STORE) {
         // dS^T row r, queries 32wg..32wg+31 of this 64-query half: chunks 4wg..4wg+3
         const uint32_t dsb = sbase + kSmemDS0 + dsbuf * kDSHalf;
 #pragma unroll
@@ -494,12 +510,19 @@ int launch_bwd_keys(const Dims& d, const DevCtx& ctx, const uint16_t* q, const u
   cudaGetDevice(&dev);
   static cudaError_t attr_status[64];
   std::call_once(attr_once[dev & 63], [dev] {
-    attr_status[dev & 63] = cudaFuncSetAttribute(bwd_keys_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    attr_status[dev & 63] = cudaFuncSetAttribute(
+        bwd_keys_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (attr_status[dev & 63] == cudaSuccess)
+      attr_status[dev & 63] = cudaFuncSetAttribute(
+          bwd_keys_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr_status[dev & 63] != cudaSuccess) return cuda_status(attr_status[dev & 63]);
   KeysArgs args{d, lse, delta, ws, dk, dvt, ctx.err, ctx.wait_ns, pk, pv};
   dim3 grid(d.kv_count, d.nt, d.B);
-  bwd_keys_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, args);
+  if (ws != nullptr)
+    bwd_keys_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, args);
+  else
+    bwd_keys_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, args);
   return cuda_status(cudaGetLastError());
 }
 
