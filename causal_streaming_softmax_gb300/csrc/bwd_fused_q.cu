@@ -325,14 +325,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; ok && j < n_kt; ++j) {
       const int pb = j & 1;
       const int k0 = j * kBN + 32 * wg;  // this thread's first key
-      if (!mbar_wait_warp(BAR(BAR_S_FULL), j & 1, wc)) {
-        ok = false;
-        break;
-      }
-      // pair buffer pb was last read by dQ += dS K of tile j-2
-      if (j >= 2 && !mbar_wait_warp(BAR(BAR_PK_FREE + pb), ((j >> 1) - 1) & 1, wc)) {
-        ok = false;
-        break;
+      // S and dP of tile j done; pair buffer pb last read by dQ += dS K of
+      // tile j-2: one vote for both, bounded waits only when one is not ready
+      {
+        const bool f1 = mbar_try_wait(BAR(BAR_S_FULL), j & 1);
+        const bool f2 = j < 2 || mbar_try_wait(BAR(BAR_PK_FREE + pb), ((j >> 1) - 1) & 1);
+        if (!__all_sync(0xffffffffu, f1 && f2)) {
+          if (!mbar_wait_warp(BAR(BAR_S_FULL), j & 1, wc)) {
+            ok = false;
+            break;
+          }
+          if (j >= 2 && !mbar_wait_warp(BAR(BAR_PK_FREE + pb), ((j >> 1) - 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+        }
       }
       tc_fence_after();
       {
