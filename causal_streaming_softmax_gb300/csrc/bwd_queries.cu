@@ -127,8 +127,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (j >= kStages && !mbar_wait(BAR(BAR_EMPTY + s), ((j / kStages) - 1) & 1, wc)) break;
         const uint32_t st = sbase + s * kStageBytes;
         mbar_arrive_expect_tx(BAR(BAR_FULL + s), kStageBytes);
-        bulk_load(st, a.ws + (size_t)(tile0 + d.pair(it, j)) * kDsTileBytes, kDsTileBytes,
-                  BAR(BAR_FULL + s));
+        // dS is read once: evict it first, so the K tiles every query tile
+        // reads again stay in L2
+        bulk_load_hint(st, a.ws + (size_t)(tile0 + d.pair(it, j)) * kDsTileBytes, kDsTileBytes,
+                       BAR(BAR_FULL + s), l2_policy_evict_first());
         tma_load_3d(st + kDsTileBytes, &tm_k, BAR(BAR_FULL + s), 0, j * kBN, kvplane);
         issued = j + 1;
       }
