@@ -118,50 +118,86 @@ def recorded_traffic(kernel_file: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons, sampled while the GPU works.
+
+    A reader thread stamps each sample with the host clock, so that only the
+    samples taken inside a marked window (the loaded region) are summarised.
+    """
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, device_index: int, period_ms: int = 50):
+        import threading
         self.proc = None
         self.err = None
+        self.samples = []  # (host time, line)
+        self.period_ms = period_ms
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(device_index), "--query-gpu=" + self.FIELDS,
                  "--format=csv,noheader,nounits", "-lms", str(period_ms)],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except (OSError, ValueError) as e:
             self.err = str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
 
-    def stop(self) -> dict:
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.perf_counter(), line))
+
+    def wait_first_sample(self, timeout_s: float = 5.0) -> bool:
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.samples:
+            if time.perf_counter() - t0 > timeout_s:
+                return False
+            time.sleep(0.01)
+        return bool(self.samples)
+
+    def stop(self, window=None) -> dict:
+        """Summary of the samples whose host time lies in ``window`` (t0, t1),
+        or of all samples."""
         if self.proc is None:
-            return dict(sm_mhz=None, sm_max_mhz=None, reasons=[], note=self.err)
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=[], samples=0, note=self.err)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=10)
+            self.proc.wait(timeout=10)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, smax, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in out.splitlines():
+            self.proc.wait()
+        self.thread.join(timeout=5)
+        return self.summarise(self.samples, window, self.period_ms)
+
+    @classmethod
+    def summarise(cls, samples, window=None, period_ms=None) -> dict:
+        """Median SM clock, the largest maximum clock, median power and the
+        throttle reasons seen, over the (host time, csv line) samples whose
+        time lies inside ``window``."""
+        sm, smax, power, reasons = [], [], [], set()
+        for t, line in samples:
+            if window is not None and not (window[0] <= t <= window[1]):
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
                 sm.append(float(parts[1]))
                 smax.append(float(parts[2]))
+                power.append(float(parts[3]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            for n, v in zip(cls.NAMES, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return dict(sm_mhz=None, sm_max_mhz=None, reasons=[], samples=0)
         return dict(sm_mhz=float(statistics.median(sm)), sm_max_mhz=float(max(smax)),
-                    reasons=sorted(reasons), samples=len(sm))
+                    sm_mhz_min=float(min(sm)), power_w_median=float(statistics.median(power)),
+                    reasons=sorted(reasons), samples=len(sm), period_ms=period_ms)
 
 
 def dist_setup():
@@ -306,13 +342,37 @@ def run_ours(args, w, world, rank, local):
     if api.last_device_error(stream) != 0:
         raise RuntimeError("device error during warm-up")
 
+    def one_step():
+        flush.zero_()
+        for _, _, fn in calls:
+            fn()
+
+    # Clocks are sampled from the start of a sustained leg (the same step back
+    # to back for --sustain-s seconds, so that the clocks and the power draw
+    # settle at their loaded level) to the end of the timed steps; only the
+    # samples inside that loaded window are summarised.
+    clocks = ClockSampler(local)
+    clocks.wait_first_sample()
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    t_load0 = time.perf_counter()
+    es0 = torch.cuda.Event(enable_timing=True)
+    es1 = torch.cuda.Event(enable_timing=True)
+    es0.record(stream)
+    n_sus = 0
+    while n_sus == 0 or time.perf_counter() - t_load0 < args.sustain_s:
+        for _ in range(20):
+            one_step()
+        n_sus += 20
+    es1.record(stream)
+    torch.cuda.synchronize(dev)
+    sus_ms = es0.elapsed_time(es1)
+
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
           for _ in range(K)]
     dist_barrier(world)
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local)
-    time.sleep(0.3)  # let the sampler start before the timed region
     t_wall0 = time.perf_counter()
     for i in range(K):
         flush.zero_()
@@ -321,9 +381,10 @@ def run_ours(args, w, world, rank, local):
             fn()
             ev[i][c + 1].record(stream)
     torch.cuda.synchronize(dev)
-    t_wall = time.perf_counter() - t_wall0
+    t_wall1 = time.perf_counter()
+    t_wall = t_wall1 - t_wall0
     dist_barrier(world)
-    clk = clocks.stop()
+    clk = clocks.stop(window=(t_load0, t_wall1))
     if api.last_device_error(stream) != 0:
         raise RuntimeError("device error during the timed steps")
 
@@ -334,9 +395,19 @@ def run_ours(args, w, world, rank, local):
     ms_per_step = total_ms / K
     fl = useful_flops(w, lens_np)
     value = world * fl["step"] * K / (total_ms / 1e3) / 1e12
+    sustained = dict(
+        what="the same step (L2 flush + the four calls) back to back under the clock sampler, "
+             "just before the timed steps; time includes the flushes",
+        steps=n_sus, seconds=sus_ms / 1e3, ms_per_step=sus_ms / n_sus,
+        value=fl["step"] / (sus_ms / n_sus / 1e3) / 1e12, unit="TFLOP/s")
+    if clk.get("sm_mhz"):
+        # device time x median loaded SM clock: thousands of SM cycles per step
+        clk["kcycles_per_step"] = ms_per_step * clk["sm_mhz"]
+        clk["window"] = "sustained leg + timed steps (%.1f s)" % (t_wall1 - t_load0)
 
     peaks = load_peaks()
     mean_ms = {n: sum(v) / K for n, v in per_call.items()}
+    median_ms = {n: float(statistics.median(v)) for n, v in per_call.items()}
     dom = max(mean_ms, key=mean_ms.get)
     dom_file = dict((n, f) for n, f, _ in calls)[dom]
     nbytes = algorithmic_bytes(w, lens_np)
@@ -357,7 +428,7 @@ def run_ours(args, w, world, rank, local):
     kernels = {}
     for n, f, _ in calls:
         k_ms = mean_ms[n]
-        e = dict(ms=k_ms, share=k_ms / sum(mean_ms.values()),
+        e = dict(ms=k_ms, ms_median=median_ms[n], share=k_ms / sum(mean_ms.values()),
                  gbs=nbytes[n] / (k_ms / 1e3) / 1e9)
         if fl[n] > 0:
             e["tflops"] = fl[n] / (k_ms / 1e3) / 1e12
@@ -441,7 +512,8 @@ def run_ours(args, w, world, rank, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, heads, secs, threads = cpu_oracle_sample(w, inp, args.cpu_budget)
-        cpu = dict(value=rate / 1e12, unit="TFLOP/s", cores=threads, kind="oracle",
+        cpu = dict(value=rate / 1e12, unit="TFLOP/s", cores=threads,
+                   host_cores=os.cpu_count(), kind="oracle",
                    sample="%d query head(s) of the %s workload, full forward + backward in "
                           "binary64, %.1f s" % (heads, w.name, secs))
 
@@ -452,8 +524,9 @@ def run_ours(args, w, world, rank, local):
                     data="synthetic (seeded normal inputs)", config=config_dict(w, lens_np),
                     parallelism="replicas" if world > 1 else "single",
                     frac_of_peak=value / world / peaks["tflops"],
+                    ms_per_step_median=float(statistics.median(step_ms)),
                     gpu_launches=len(calls) * K, kernels=kernels, roofline=roof,
-                    clocks=clk, e2e=e2e, cpu_baseline=cpu, fused_dq_variant=variant,
+                    clocks=clk, sustained=sustained, e2e=e2e, cpu_baseline=cpu, fused_dq_variant=variant,
                     wall_s_timed=t_wall)
         print(json.dumps(line))
     return 0
@@ -470,11 +543,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip timing the fused-dQ variant of the step")
+    ap.add_argument("--sustain-s", type=float, default=2.0,
+                    help="seconds of back-to-back steps under the clock sampler before "
+                         "the timed steps")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for cpu_baseline")
     args = ap.parse_args()
     # at least three untimed warm-up steps, whatever was asked
     args.warmup = max(3, args.warmup)
+    args.sustain_s = max(0.0, args.sustain_s)
     world, rank, local = dist_setup()
     if world != args.gpus and world > 1:
         print("warning: WORLD_SIZE=%d, --gpus=%d" % (world, args.gpus), file=sys.stderr)

@@ -26,6 +26,10 @@ ATTN_ERR_WORKSPACE = -4
 ATTN_ERR_CUDA = -5
 ATTN_ERR_DEVICE_TIMEOUT = -6
 ATTN_ERR_DEVICE = -7
+ATTN_ERR_SCRATCH_LIMIT = -8
+
+# lowest bounded-wait limit the library accepts (attn_set_wait_limit_ns)
+MIN_WAIT_LIMIT_NS = 10_000_000
 
 HEAD_DIM = 64
 
@@ -94,6 +98,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attn_last_device_error.argtypes = [vp]
     lib.attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.attn_set_wait_limit_ns.restype = None
+    lib.attn_wait_limit_ns.argtypes = []
+    lib.attn_wait_limit_ns.restype = ctypes.c_uint64
     lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.attn_version.restype = ctypes.c_int
     lib.attn_last_cuda_error.restype = ctypes.c_char_p
@@ -327,7 +333,13 @@ def check_device_error(stream=None) -> None:
 
 
 def set_wait_limit_ns(ns: int) -> None:
+    """Sets the kernels' bounded-wait limit (0: the default; values below
+    MIN_WAIT_LIMIT_NS are raised to it)."""
     load_library().attn_set_wait_limit_ns(int(ns))
+
+
+def wait_limit_ns() -> int:
+    return int(load_library().attn_wait_limit_ns())
 
 
 def selftest_arith(x, stream=None):

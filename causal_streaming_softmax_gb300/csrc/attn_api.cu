@@ -172,8 +172,12 @@ const char* attn_error_string(int code) {
 }
 
 void attn_set_wait_limit_ns(uint64_t limit_ns) {
-  g_wait_ns.store(limit_ns ? limit_ns : kDefaultWaitNs, std::memory_order_relaxed);
+  uint64_t v = limit_ns ? limit_ns : kDefaultWaitNs;
+  if (v < ATTN_MIN_WAIT_LIMIT_NS) v = ATTN_MIN_WAIT_LIMIT_NS;
+  g_wait_ns.store(v, std::memory_order_relaxed);
 }
+
+uint64_t attn_wait_limit_ns(void) { return g_wait_ns.load(std::memory_order_relaxed); }
 
 size_t attn_bwd_workspace_bytes(const attn_shape* shape) {
   Dims d;

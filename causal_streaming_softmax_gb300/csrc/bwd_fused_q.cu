@@ -89,13 +89,6 @@ struct FusedArgs {
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
-static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > limit_ns) return false;
-  return true;
-}
-
 // dS = P (dP - D) with P = 2^(S c - L) for 32 keys of one query row, packed
 // to binary16 pairs.  MASK zeroes the keys outside [0, lim) (local indices).
 template <bool MASK>
@@ -203,9 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         issued = j + 1;
       }
-      drain_wait(BAR(BAR_QD_FULL), 0, a.wait_ns);
+      drain_wait(BAR(BAR_QD_FULL), 0);
       for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
-        drain_wait(BAR(BAR_KV_FULL + j % kStages), (j / kStages) & 1, a.wait_ns);
+        drain_wait(BAR(BAR_KV_FULL + j % kStages), (j / kStages) & 1);
     }
   } else if (warp >= 17) {
     // ---------------- MMA issuers ----------------
@@ -368,7 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait_warp(BAR(BAR_DONE), 0, wc) && ok;
         tc_fence_after();
         uint32_t r0[16];
-        tmem_ld16_wait(tmem + lane_base + kColDQ + 16 * wg, r0);
+        // ok is warp-uniform; after a wait gave up the load is skipped
+        if (ok) {
+          tmem_ld16_wait(tmem + lane_base + kColDQ + 16 * wg, r0);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) r0[u] = 0u;
+        }
         float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -381,9 +380,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (n_kt > 0) {
       ok = mbar_wait_warp(BAR(BAR_DONE), 0, wc) && ok;
-      tc_fence_after();
-      uint32_t r0[16];
-      tmem_ld16_wait(tmem + lane_base + kColDQ + 16 * wg, r0);
     }
     (void)ok;
   }
@@ -392,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 17) {
     tc_fence_after();
-    if (n_kt > 0) drain_wait(BAR(BAR_DONE), 0, a.wait_ns);
+    if (n_kt > 0) drain_wait(BAR(BAR_DONE), 0);
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -102,13 +102,6 @@ struct KeysArgs {
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
-static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > limit_ns) return false;
-  return true;
-}
-
 // One key row's step for 32 queries: P = 2^(S c - L) and dS = P (dP - D),
 // both packed to binary16 pairs (P for dV, dS for dK and the workspace); dS
 // takes P unrounded.  MASK zeroes P, so also dS, outside [qlo, qhi) (local
@@ -245,9 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = n + 1;
         if (++rem == per_g) rem = 0, ++g;
       }
-      drain_wait(BAR(BAR_KV_FULL), 0, a.wait_ns);
+      drain_wait(BAR(BAR_KV_FULL), 0);
       for (int n = (issued > kStages ? issued - kStages : 0); n < issued; ++n)
-        drain_wait(BAR(BAR_Q_FULL + n % kStages), (n / kStages) & 1, a.wait_ns);
+        drain_wait(BAR(BAR_Q_FULL + n % kStages), (n / kStages) & 1);
     }
   } else if (warp == 13) {
     // ---------------- store: dS^T of each step into the workspace ----------------
@@ -446,8 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue: dK = s * sum (rows), dV^T (columns) ----------------
     const bool store = key < T;
     uint32_t r0[32], r1[32];
-    if (n_steps > 0) {
-      ok = ok && mbar_wait(BAR(BAR_DONE), 0, wc);
+    // ok is warp-uniform (every wait above is taken by the whole warp); the
+    // epilogue wait is too, so the warp-aligned load runs converged, and it
+    // is skipped once any wait gave up
+    if (n_steps > 0 && ok && mbar_wait_warp(BAR(BAR_DONE), 0, wc)) {
       tc_fence_after();
       const uint32_t col = wg == 0 ? kColDK : kColDV;
       tmem_ld32x2_wait(tmem + lane_base + col, tmem + lane_base + col + 32, r0, r1);
@@ -484,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 9) {
     tc_fence_after();
-    if (n_steps > 0) drain_wait(BAR(BAR_DONE), 0, a.wait_ns);
+    if (n_steps > 0) drain_wait(BAR(BAR_DONE), 0);
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -59,13 +59,6 @@ struct QueriesArgs {
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
-static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > limit_ns) return false;
-  return true;
-}
-
 // EPI: 0 binary32 dQ rows [B][H][T][64]; 1 the inverse half-split rotation
 // to bfloat16 token-major; 2 the projection-fused token-major block.
 template <int EPI>
@@ -135,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         issued = j + 1;
       }
       for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
-        drain_wait(BAR(BAR_FULL + j % kStages), (j / kStages) & 1, a.wait_ns);
+        drain_wait(BAR(BAR_FULL + j % kStages), (j / kStages) & 1);
     }
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
@@ -161,8 +154,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int q = q0 + threadIdx.x;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     uint32_t r0[32], r1[32];
-    if (n_kt > 0) {
-      mbar_wait(BAR(BAR_DONE), 0, wc);
+    // the whole warp waits together, so the warp-aligned tensor-memory load
+    // below runs converged; if the wait gave up, the load is skipped (the
+    // device error word already records the timeout)
+    if (n_kt > 0 && mbar_wait_warp(BAR(BAR_DONE), 0, wc)) {
       tc_fence_after();
       tmem_ld32x2_wait(tmem + lane_base, tmem + lane_base + 32, r0, r1);
     } else {
@@ -221,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
-    if (n_kt > 0) drain_wait(BAR(BAR_DONE), 0, a.wait_ns);
+    if (n_kt > 0) drain_wait(BAR(BAR_DONE), 0);
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -78,15 +78,6 @@ struct FwdArgs {
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
-// Waits used only to drain in-flight asynchronous work before the CTA exits
-// (they ignore the abort flag; bounded by the same limit).
-static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > limit_ns) return false;
-  return true;
-}
-
 // Number of 128-key tiles that query rows [q0, q0 + 128) see.
 __device__ __forceinline__ int key_tiles(int q0, int len, int causal) {
   if (q0 >= len) return 0;
@@ -271,9 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // no copy may still be landing when the CTA exits (matters only when a
       // wait gave up): wait for Q and the last fill of each stage
-      drain_wait(BAR(BAR_Q), 0, a.wait_ns);
+      drain_wait(BAR(BAR_Q), 0);
       for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
-        drain_wait(BAR(BAR_KV_FULL + j % kStages), (j / kStages) & 1, a.wait_ns);
+        drain_wait(BAR(BAR_KV_FULL + j % kStages), (j / kStages) & 1);
     }
   } else if (warp >= 9) {
     // ---------------- MMA issuers: one thread per product chain ----------------
@@ -415,7 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = ok && mbar_wait_warp(BAR(BAR_O_DONE + t), 0, wc);
       tc_fence_after();
       uint32_t o0[32], o1[32];
-      tmem_ld32x2_wait(t_o, t_o + 32, o0, o1);
+      // ok is warp-uniform; after a wait gave up the load is skipped
+      if (ok) {
+        tmem_ld32x2_wait(t_o, t_o + 32, o0, o1);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) o0[u] = o1[u] = 0u;
+      }
       const bool valid = row_ok && l > 0.f;
       const float inv = valid ? 1.0f / l : 0.f;
       if (qrow < T) {
@@ -449,10 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 9) {
     tc_fence_after();
     // every MMA of this CTA has completed before its tensor memory is freed
-    if (n_a > 0) drain_wait(BAR(BAR_O_DONE), 0, a.wait_ns);
-    if (n_b > 0) drain_wait(BAR(BAR_O_DONE + 1), 0, a.wait_ns);
-    if (n_a > 0) drain_wait(BAR(BAR_S_FULL), (n_a - 1) & 1, a.wait_ns);
-    if (n_b > 0) drain_wait(BAR(BAR_S_FULL + 1), (n_b - 1) & 1, a.wait_ns);
+    if (n_a > 0) drain_wait(BAR(BAR_O_DONE), 0);
+    if (n_b > 0) drain_wait(BAR(BAR_O_DONE + 1), 0);
+    if (n_a > 0) drain_wait(BAR(BAR_S_FULL), (n_a - 1) & 1);
+    if (n_b > 0) drain_wait(BAR(BAR_S_FULL + 1), (n_b - 1) & 1);
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }

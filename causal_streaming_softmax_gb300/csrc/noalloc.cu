@@ -4,8 +4,11 @@
 //
 // The array below is a host-side stand-in in host code, not a device
 // address: host code must never hand its name to a kernel.  Its device
-// address is looked up with cudaGetSymbolAddress once per device (with that
-// device current) and cached; that pointer is what the kernels receive.
+// address is looked up with cudaGetSymbolAddress, with the device current,
+// the first time a call runs in a device's context, and cached per context:
+// a device reset (or a released and re-created primary context) loads the
+// module again, possibly at another address, so a new context looks the
+// address up again.  A failed lookup is not cached.
 #include <mutex>
 
 #include "attn_internal.h"
@@ -15,25 +18,56 @@ namespace {
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <class F>
+F driver_fn(const char* name, int version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(p);
+}
+
+// Unique id of the calling thread's current context (0 if none or unknown).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 4000);
+  static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
 constexpr int kMaxDevices = 64;
 struct ScratchSlot {
-  std::once_flag once;
-  cudaError_t status = cudaErrorUnknown;
+  unsigned long long ctx_id = 0;  // context the cached address belongs to
   uint8_t* ptr = nullptr;
 };
 ScratchSlot g_slots[kMaxDevices];
+std::mutex g_slots_mu;
 
-// Device address of the scratch on the current device.
+// Device address of the scratch in the current device's current context.
 int scratch_address(uint8_t** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_DEVICE;
+  const unsigned long long id = current_context_id();
+  std::lock_guard<std::mutex> lock(g_slots_mu);
   ScratchSlot& slot = g_slots[dev];
-  std::call_once(slot.once, [&slot] {
+  if (id == 0 || slot.ptr == nullptr || slot.ctx_id != id) {
     void* p = nullptr;
-    slot.status = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (p == nullptr) return ATTN_ERR_CUDA;
     slot.ptr = static_cast<uint8_t*>(p);
-  });
-  if (slot.status != cudaSuccess || slot.ptr == nullptr) return ATTN_ERR_CUDA;
+    slot.ctx_id = id;
+  }
   *out = slot.ptr;
   return ATTN_OK;
 }

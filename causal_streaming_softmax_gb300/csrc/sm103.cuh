@@ -139,6 +139,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   return mbar_wait_slow(bar, parity, w);
 }
 
+// Bounded wait used only to drain asynchronous work this CTA issued (copies,
+// MMAs) before it frees tensor memory or exits.  It ignores the abort flag
+// and uses its own fixed limit, independent of the caller's wait limit, so
+// a short caller limit can never free tensor memory or end the CTA while a
+// copy or an MMA that targets it is still in flight.  It runs out only when
+// the awaited operation was never issued (after another wait gave up).
+constexpr uint64_t kDrainLimitNs = 4000000000ull;  // 4 s
+
+static __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kDrainLimitNs) return false;
+  return true;
+}
+
 // The same wait taken by a whole converged warp: true only if every lane's
 // wait succeeded, so the warp leaves together and never splits around a
 // .sync.aligned tensor-memory instruction.

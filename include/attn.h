@@ -313,8 +313,10 @@ ATTN_API int attn_bwd_queries_projected(const attn_shape* shape, const uint16_t*
  * which the library's code is loaded holds that array until the process
  * exits.  The call walks the chunk's K/V heads in groups that fit the array,
  * and calls no cudaMalloc, cudaFree or other allocating routine.  The first
- * call on a device looks up the array's device address (once per device,
- * with that device current); make that first call before any stream capture.
+ * call in a device's context looks up the array's device address (with that
+ * device current) and keeps it for that context; after a device reset the
+ * next call looks it up again.  Make the first call on each device before
+ * any stream capture.
  *
  * Arguments as attn_bwd_keys and attn_bwd_queries (device pointers, 16-byte
  * aligned, layouts in the file header): reads q, k, vt, dout, lse, delta;
@@ -350,16 +352,25 @@ ATTN_API int attn_last_device_error(void* stream);
 /*
  * Sets the time limit of every bounded wait inside the kernels launched
  * afterwards on any device (nanoseconds; 0 restores the default of 2 s).
- * Not part of the method: a safety bound so that a kernel never spins
- * forever.
+ * Values below ATTN_MIN_WAIT_LIMIT_NS (10 ms) are raised to it, so that no
+ * ordinary pipeline wait gives up on a busy GPU.  The waits that drain a
+ * kernel's own copies and products before it frees tensor memory or exits
+ * keep their own fixed limit, whatever is set here.  Not part of the method:
+ * a safety bound so that a kernel never spins forever.
  */
+#define ATTN_MIN_WAIT_LIMIT_NS ((uint64_t)10000000)
 ATTN_API void attn_set_wait_limit_ns(uint64_t limit_ns);
+
+/* The bounded-wait limit that kernels launched now would use (nanoseconds). */
+ATTN_API uint64_t attn_wait_limit_ns(void);
 
 /*
  * Self-test of the bounded wait: launches one block that waits on a barrier
- * nothing will complete, with a limit of limit_ns, then synchronises and
- * returns what attn_last_device_error reports (ATTN_ERR_DEVICE_TIMEOUT when
- * the wait gave up as it should).  Not part of the method.
+ * nothing will complete, with a limit of limit_ns (its own, not the one set
+ * above; 0 means 1 ms), then synchronises and returns what
+ * attn_last_device_error reports (ATTN_ERR_DEVICE_TIMEOUT when the wait gave
+ * up as it should).  The probe issues no copy or product, so its short limit
+ * is safe.  Not part of the method.
  */
 ATTN_API int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream);
 

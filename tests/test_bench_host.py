@@ -86,3 +86,19 @@ def test_peaks_come_from_the_measured_file():
         assert p["source"] == "measured" and p["tflops"] > 0 and p["hbm_gbs"] > 0
     else:
         assert p["source"] == "fallback"
+
+
+def test_clock_summary_keeps_only_the_loaded_window():
+    """Samples outside the loaded window (an idle GPU before or after) do not
+    enter the clock summary; throttle reasons inside it are reported."""
+    line = "0, {sm}, 2070, {pw}, 0x0, Not Active, Not Active, Not Active, {cap}\n"
+    samples = [(0.0, line.format(sm=2070, pw=200, cap="Not Active")),      # idle, before
+               (1.0, line.format(sm=1800, pw=900, cap="Not Active")),
+               (1.1, line.format(sm=1700, pw=1300, cap="Active")),
+               (1.2, line.format(sm=1750, pw=1200, cap="Not Active")),
+               (9.0, line.format(sm=2070, pw=150, cap="Not Active"))]      # idle, after
+    c = bench.ClockSampler.summarise(samples, window=(0.5, 2.0), period_ms=50)
+    assert c["samples"] == 3
+    assert c["sm_mhz"] == 1750.0 and c["sm_mhz_min"] == 1700.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"]
+    assert bench.ClockSampler.summarise(samples, window=(3.0, 4.0))["samples"] == 0

@@ -138,3 +138,28 @@ def test_step_host_rejections(lib):
     short = api.AttnDeviceBuffers(p, p, p, p, p, p, p, p, 16, p, p, p)
     assert lib.attn_step_host(ctypes.byref(s), ctypes.byref(short), *h, p, None) == \
         api.ATTN_ERR_WORKSPACE
+
+
+def test_wait_limit_has_a_floor(lib):
+    """The bounded-wait limit reads back as set, is raised to the floor when
+    set lower, and 0 restores the default; no GPU is touched."""
+    default = api.wait_limit_ns()
+    try:
+        api.set_wait_limit_ns(3_000_000_000)
+        assert api.wait_limit_ns() == 3_000_000_000
+        for tiny in (1, 1000, api.MIN_WAIT_LIMIT_NS - 1):
+            api.set_wait_limit_ns(tiny)
+            assert api.wait_limit_ns() == api.MIN_WAIT_LIMIT_NS
+        api.set_wait_limit_ns(0)
+        assert api.wait_limit_ns() == 2_000_000_000
+    finally:
+        api.set_wait_limit_ns(default)
+
+
+def test_header_constants_match_binding():
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    codes = dict(re.findall(r"(ATTN_(?:OK|ERR_\w+))\s*=\s*(-?\d+)", text))
+    for name, value in codes.items():
+        assert getattr(api, name) == int(value), name
+    floor = re.search(r"ATTN_MIN_WAIT_LIMIT_NS\s+\(\(uint64_t\)(\d+)\)", text)
+    assert floor and int(floor.group(1)) == api.MIN_WAIT_LIMIT_NS

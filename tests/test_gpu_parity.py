@@ -181,6 +181,24 @@ def _check_sampled(w, inp, gpu, heads, kv_heads, batches, rng):
     return worst
 
 
+def _sample_plan(w, inp, gpu):
+    """Which batches, query heads and K/V heads a full-size workload is
+    sampled on; for length-masked workloads also checks that every row and
+    key at or past a sequence's length got exact zeros."""
+    B, H, G = w.batch, w.heads, w.group
+    lens = inp["lens"]
+    if lens is None:
+        return [0], [0, G - 1, H - 1], [w.kv_heads - 1]
+    for b in range(B):
+        n = int(lens[b])
+        assert np.all(gpu["dk"][b, :, n:] == 0.0)
+        assert np.all(gpu["dvt"][b, :, :, n:] == 0.0)
+        assert np.all(gpu["dq"][b, :, n:] == 0.0)
+        assert np.all(gpu["delta"][b, :, n:] == 0.0)
+    batches = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 0, B - 1})
+    return batches, [0, H - 1], [0]
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("cfg", [3, 4, 5])
 def test_workload_sampled(cuda_device, cfg):
@@ -188,22 +206,7 @@ def test_workload_sampled(cuda_device, cfg):
     inp = workloads.make_inputs(w)
     gpu = run_gpu(inp, causal=w.causal, scale=w.scale)
     rng = np.random.default_rng(100 + cfg)
-    B, H = w.batch, w.heads
-    G = w.group
-    if cfg == 4:
-        lens = inp["lens"]
-        batches = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 0, B - 1})
-        heads, kv_heads = [0, H - 1], [0]
-        # keys at or past a sequence's length have dK = dV = 0 exactly
-        for b in range(B):
-            n = int(lens[b])
-            assert np.all(gpu["dk"][b, :, n:] == 0.0)
-            assert np.all(gpu["dvt"][b, :, :, n:] == 0.0)
-            assert np.all(gpu["dq"][b, :, n:] == 0.0)
-    else:
-        batches = [0]
-        heads = [0, G - 1, H - 1]
-        kv_heads = [w.kv_heads - 1]
+    batches, heads, kv_heads = _sample_plan(w, inp, gpu)
     _check_sampled(w, inp, gpu, heads, kv_heads, batches, rng)
 
 
@@ -300,14 +303,14 @@ def test_key_pass_without_store_same_bits(cuda_device):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("cfg", [3, 5])
+@pytest.mark.parametrize("cfg", [3, 4, 5])
 def test_fused_dq_workload_sampled(cuda_device, cfg):
     w = workloads.WORKLOADS[cfg]
     inp = workloads.make_inputs(w)
     gpu = run_gpu(inp, causal=w.causal, scale=w.scale, fused_dq=True)
     rng = np.random.default_rng(200 + cfg)
-    G = w.group
-    _check_sampled(w, inp, gpu, [0, G - 1, w.heads - 1], [w.kv_heads - 1], [0], rng)
+    batches, heads, kv_heads = _sample_plan(w, inp, gpu)
+    _check_sampled(w, inp, gpu, heads, kv_heads, batches, rng)
 
 
 def test_fused_dq_head_chunks_match_whole(cuda_device):
@@ -403,7 +406,8 @@ def test_rotated_dq(cuda_device, B, T, H, Hkv, causal, lens):
 def test_projection_epilogues(cuda_device, B, T, H, Hkv, causal, lens, store_ds):
     """The projection blocks hold exactly the plain passes' dQ, dK and dV
     (dV untransposed) in binary32, their round-to-nearest-even bfloat16, and
-    nothing outside the blocks changes."""
+    nothing outside the blocks changes; both blocks also match the oracle's
+    gradients laid out token-major within the gradient tolerance."""
     import torch
     from causal_streaming_softmax_gb300 import api
     inp = workloads.make_custom_inputs(B, T, H, Hkv, causal=causal, lens=lens, seed=T + H)
@@ -433,6 +437,16 @@ def test_projection_epilogues(cuda_device, B, T, H, Hkv, causal, lens, store_ds)
         n = want.shape[2]
         assert np.array_equal(a32[:, :, c0:c0 + n], want)
         assert np.array_equal(a16[:, :, c0:c0 + n], _bf16_rne(want))
+    # and against the oracle directly, in the same token-major layout: the
+    # blocks must be the gradients, not only equal to another CUDA pass
+    ref = _full(inp, causal)
+    ref_q = ref["dq"].transpose(0, 2, 1, 3).reshape(B, T, H * 64)
+    ref_k = ref["dk"].transpose(0, 2, 1, 3).reshape(B, T, Hkv * 64)
+    ref_v = ref["dvt"].transpose(0, 3, 1, 2).reshape(B, T, Hkv * 64)
+    for c0, want in ((cq, ref_q), (ck, ref_k), (cv, ref_v)):
+        n = want.shape[2]
+        assert rel_fro(a32[:, :, c0:c0 + n], want) <= GRAD_TOL
+        assert rel_fro(a16[:, :, c0:c0 + n], want) <= GRAD_TOL
     for arr in (a32, a16):
         assert np.all(arr[:, :, :cq] == -3.0) and np.all(arr[:, :, cv + Hkv * 64:] == -3.0)
 

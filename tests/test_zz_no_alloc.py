@@ -101,5 +101,5 @@ def test_noalloc_refuses_oversized_shape(cuda_device):
     rc = fn(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), vt.data_ptr(), dout.data_ptr(),
             lse.data_ptr(), delta.data_ptr(), dq.data_ptr(), dk.data_ptr(), dvt.data_ptr(),
             torch.cuda.current_stream().cuda_stream)
-    assert rc == -8, api.error_string(rc)  # ATTN_ERR_SCRATCH_LIMIT
+    assert rc == api.ATTN_ERR_SCRATCH_LIMIT, api.error_string(rc)
     assert "static scratch" in api.error_string(rc)
