@@ -45,6 +45,10 @@ EDGE = [
     # empty sequences in a batch: no row and no key of theirs is valid
     (3, 256, 4, 2, True, [0, 100, 256]),
     (2, 128, 2, 1, False, [0, 128]),
+    # more forward work units (256 queries of a head) than SMs: the persistent
+    # forward walks several units per CTA; the last block's second query tile
+    # holds no row (T = 576)
+    (1, 576, 80, 8, True, None),
 ]
 
 
