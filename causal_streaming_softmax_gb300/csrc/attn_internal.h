@@ -70,6 +70,28 @@ bool encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1
 // attn_last_cuda_error on this host thread and returns ATTN_ERR_CUDA.
 int cuda_status(cudaError_t e);
 
+// Launches `kernel` with programmatic stream serialization: it may start
+// while the previous kernel in `stream` finishes (every kernel of the path
+// calls griddep_wait before touching global memory).  Returns the launch's
+// status.
+template <typename... P, typename... A>
+inline cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, A&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+  const cudaError_t last = cudaGetLastError();  // takes the launch error off the thread
+  return e != cudaSuccess ? e : last;
+}
+
 int launch_fwd(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16_t* k,
                const uint16_t* vt, uint16_t* o, float* lse, cudaStream_t stream);
 int launch_row_terms(const Dims& d, const DevCtx& ctx, const uint16_t* o, const uint16_t* dout,

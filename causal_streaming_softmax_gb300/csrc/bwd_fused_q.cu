@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_vt,
                        const __grid_constant__ CUtensorMap tm_do, const FusedArgs a) {
+  griddep_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -134,15 +135,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int it = (int)gridDim.y - 1 - (int)blockIdx.y;  // heaviest causal tiles first
   const int b = blockIdx.z;
   const int T = d.T;
-  int len = T;
-  if (d.lens) {
-    len = d.lens[b];
-    len = len < 0 ? 0 : (len > T ? T : len);
-  }
-  const int q0 = it * kBM;
-  int n_kt = 0;
-  if (q0 < len) n_kt = d.causal ? it + 1 : (len + kBN - 1) / kBN;
-  if (d.causal && n_kt * kBN > len) n_kt = (len + kBN - 1) / kBN;
 
   WaitCtl wc{a.err, a.wait_ns, &s_abort};
 
@@ -168,6 +160,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  griddep_wait();
+  int len = T;
+  if (d.lens) {
+    len = d.lens[b];
+    len = len < 0 ? 0 : (len > T ? T : len);
+  }
+  const int q0 = it * kBM;
+  int n_kt = 0;
+  if (q0 < len) n_kt = d.causal ? it + 1 : (len + kBN - 1) / kBN;
+  if (d.causal && n_kt * kBN > len) n_kt = (len + kBN - 1) / kBN;
 
   if (warp == 16) {
     // ---------------- TMA producer ----------------
@@ -419,8 +421,8 @@ int launch_bwd_fused_q(const Dims& d, const DevCtx& ctx, const uint16_t* q, cons
   if (attr_status[dev & 63] != cudaSuccess) return cuda_status(attr_status[dev & 63]);
   FusedArgs args{d, o, lse, delta, dq, ctx.err, ctx.wait_ns};
   dim3 grid(d.kv_count * d.G, d.nt, d.B);
-  bwd_fused_q_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, args);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_dependent(bwd_fused_q_kernel, grid, dim3(kThreads), kSmemBytes, stream,
+                                     tq, tk, tv, tdo, args));
 }
 
 }  // namespace css

@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_vt,
                     const __grid_constant__ CUtensorMap tm_do, const KeysArgs a) {
+  griddep_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -164,21 +165,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int jt = blockIdx.y;  // key tile; low tiles see the most queries (heaviest first)
   const int b = blockIdx.z;
   const int T = d.T;
-  int len = T;
-  if (d.lens) {
-    len = d.lens[b];
-    len = len < 0 ? 0 : (len > T ? T : len);
-  }
-  const int k0 = jt * kBK;
-  const int i_lo = d.causal ? jt : 0;
-  int i_hi = (len + kTile - 1) / kTile;
-  if (k0 >= len) i_hi = i_lo;
-  const int n_i = i_hi > i_lo ? i_hi - i_lo : 0;
-  // 64-query halves per query head: the second half of a tile that starts at
-  // or past T holds no row and is skipped (its rows are never stored).
-  const bool half_tail = n_i > 0 && (i_hi - 1) * kTile + kBQ >= T;
-  const int per_g = n_i > 0 ? 2 * n_i - (half_tail ? 1 : 0) : 0;
-  const int n_steps = d.G * per_g;
 
   WaitCtl wc{a.err, a.wait_ns, &s_abort};
 
@@ -205,6 +191,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  griddep_wait();
+  int len = T;
+  if (d.lens) {
+    len = d.lens[b];
+    len = len < 0 ? 0 : (len > T ? T : len);
+  }
+  const int k0 = jt * kBK;
+  const int i_lo = d.causal ? jt : 0;
+  int i_hi = (len + kTile - 1) / kTile;
+  if (k0 >= len) i_hi = i_lo;
+  const int n_i = i_hi > i_lo ? i_hi - i_lo : 0;
+  // 64-query halves per query head: the second half of a tile that starts at
+  // or past T holds no row and is skipped (its rows are never stored).
+  const bool half_tail = n_i > 0 && (i_hi - 1) * kTile + kBQ >= T;
+  const int per_g = n_i > 0 ? 2 * n_i - (half_tail ? 1 : 0) : 0;
+  const int n_steps = d.G * per_g;
 
   if (warp == 8) {
     // ---------------- TMA producer ----------------
@@ -514,11 +516,11 @@ int launch_bwd_keys(const Dims& d, const DevCtx& ctx, const uint16_t* q, const u
   if (attr_status[dev & 63] != cudaSuccess) return cuda_status(attr_status[dev & 63]);
   KeysArgs args{d, lse, delta, ws, dk, dvt, ctx.err, ctx.wait_ns, pk, pv};
   dim3 grid(d.kv_count, d.nt, d.B);
-  if (ws != nullptr)
-    bwd_keys_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, args);
-  else
-    bwd_keys_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, args);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(
+      ws != nullptr ? launch_dependent(bwd_keys_kernel<true>, grid, dim3(kThreads), kSmemBytes,
+                                       stream, tq, tk, tv, tdo, args)
+                    : launch_dependent(bwd_keys_kernel<false>, grid, dim3(kThreads), kSmemBytes,
+                                       stream, tq, tk, tv, tdo, args));
 }
 
 }  // namespace css

@@ -64,6 +64,7 @@ __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 2)
     bwd_queries_kernel(const __grid_constant__ CUtensorMap tm_k, const QueriesArgs a) {
+  griddep_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -81,14 +82,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int it = (int)gridDim.y - 1 - (int)blockIdx.y;  // heaviest causal tiles first
   const int b = blockIdx.z;
   const int T = d.T;
-  int len = T;
-  if (d.lens) {
-    len = d.lens[b];
-    len = len < 0 ? 0 : (len > T ? T : len);
-  }
-  const int q0 = it * kBM;
-  int n_kt = 0;
-  if (q0 < len) n_kt = d.causal ? it + 1 : (len + kBN - 1) / kBN;
   const int Hc = d.ws_heads ? d.ws_heads : d.kv_count * d.G;
   const long long tile0 = ((long long)b * Hc + d.ws_h0 + h_local) * d.npairs;
 
@@ -108,6 +101,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  griddep_wait();
+  int len = T;
+  if (d.lens) {
+    len = d.lens[b];
+    len = len < 0 ? 0 : (len > T ? T : len);
+  }
+  const int q0 = it * kBM;
+  int n_kt = 0;
+  if (q0 < len) n_kt = d.causal ? it + 1 : (len + kBN - 1) / kBN;
 
   if (warp == 4) {
     // ---------------- producer: workspace tile (bulk) + K tile (TMA) ----------------
@@ -250,13 +252,10 @@ int launch_bwd_queries(const Dims& d, const DevCtx& ctx, const uint16_t* k, cons
   if (attr_status[dev & 63] != cudaSuccess) return cuda_status(attr_status[dev & 63]);
   QueriesArgs args{d, ws, dq, cos_t, sin_t, rot_out, ld, ctx.err, ctx.wait_ns, pq};
   dim3 grid(d.kv_count * d.G, d.nt, d.B);
-  if (pq.on())
-    bwd_queries_kernel<2><<<grid, kThreads, kSmemBytes, stream>>>(tk, args);
-  else if (rot_out != nullptr)
-    bwd_queries_kernel<1><<<grid, kThreads, kSmemBytes, stream>>>(tk, args);
-  else
-    bwd_queries_kernel<0><<<grid, kThreads, kSmemBytes, stream>>>(tk, args);
-  return cuda_status(cudaGetLastError());
+  auto* kernel = pq.on() ? bwd_queries_kernel<2>
+                         : (rot_out != nullptr ? bwd_queries_kernel<1> : bwd_queries_kernel<0>);
+  return cuda_status(
+      launch_dependent(kernel, grid, dim3(kThreads), kSmemBytes, stream, tk, args));
 }
 
 }  // namespace css

@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  griddep_launch_dependents();
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t bar0 = sbase + kSmemBar;
@@ -267,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  griddep_wait();
 
   if (warp == 8) {
     // ---------------- TMA producer ----------------
@@ -605,11 +607,14 @@ int launch_fwd(const Dims& d, const DevCtx& ctx, const uint16_t* q, const uint16
   // batch (2048 units) were 2% and 9% faster with one CTA per unit.
   const bool persistent = d.lens == nullptr && units <= 4LL * ctx.sm_count;
   dim3 grid((unsigned)(persistent && units > ctx.sm_count ? ctx.sm_count : units));
+  cudaError_t e;
   if (d.v_rows)
-    fwd_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, args);
+    e = launch_dependent(fwd_kernel<true>, grid, dim3(kThreads), kSmemBytes, stream, tq, tk, tv,
+                         args);
   else
-    fwd_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, args);
-  return cuda_status(cudaGetLastError());
+    e = launch_dependent(fwd_kernel<false>, grid, dim3(kThreads), kSmemBytes, stream, tq, tk, tv,
+                         args);
+  return cuda_status(e);
 }
 
 }  // namespace css

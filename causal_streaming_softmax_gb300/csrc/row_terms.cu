@@ -38,6 +38,8 @@ __device__ __forceinline__ float dot8(uint4 a, uint4 b) {
 __global__ void __launch_bounds__(kThreads)
     row_terms_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                      float* __restrict__ delta, int T, int H, const int32_t* __restrict__ lens) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int t = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 3);
   const int h = blockIdx.y;
   const int b = blockIdx.z;
@@ -99,8 +101,8 @@ int launch_row_terms(const Dims& d, const DevCtx& ctx, const uint16_t* o, const 
   (void)ctx;
   if (d.H > 65535 || d.B > 65535) return ATTN_ERR_SHAPE;
   dim3 grid(d.T / kRowsPerBlock, d.H, d.B);
-  row_terms_kernel<<<grid, kThreads, 0, stream>>>(o, dout, delta, d.T, d.H, d.lens);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_dependent(row_terms_kernel, grid, dim3(kThreads), 0, stream, o, dout,
+                                     delta, d.T, d.H, d.lens));
 }
 
 int launch_wait_probe(const DevCtx& ctx, uint64_t limit_ns, cudaStream_t stream) {

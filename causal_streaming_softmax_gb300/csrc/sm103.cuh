@@ -73,6 +73,19 @@ __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream is still
+// running; griddep_wait blocks the calling thread until that kernel has
+// completed and its memory operations are visible, so it precedes every
+// global-memory access of the kernel (a plain launch returns at once).
+// griddep_launch_dependents lets the next such kernel start once every CTA
+// of this grid has issued it or exited, so the next launch and its prologue
+// (barrier set-up, tensor-memory allocation) overlap this kernel's tail.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // bounded waits
 // ---------------------------------------------------------------------------
