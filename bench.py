@@ -13,16 +13,18 @@ non-causal length-masked workload counts 4 d H sum(len^2).
 
 Reported in one JSON line (rank 0): ``value`` is device throughput with the
 inputs resident in HBM (L2 flushed before every timed step by a 256 MiB
-write, outside the timed events), ``e2e`` the same metric through the
-host-buffer C-ABI call attn_step_host (pinned host -> device copies, the
-four kernels, device -> host copies of O, L, dQ, dK, dV^T, all inside the
-timed region, the copies overlapped with the kernels),
-``roofline`` the dominant kernel against the measured tensor peak,
+write, outside the timed events, which sit at step boundaries only; the
+per-call split comes from a second leg with an event after every call),
+``e2e`` the same metric through the host-buffer C-ABI call attn_step_host
+(pinned host -> device copies, the kernels, device -> host copies of O, L,
+dQ, dK, dV^T, all inside the timed region, the copies overlapped with the
+kernels; ``order`` says whether the call took the stored or the fused
+order), ``roofline`` the dominant kernel against the measured tensor peak,
 ``cpu_baseline`` the binary64 oracle on a bounded sample timed on the host,
 and ``fused_dq_variant`` the same step as the pages' two-launch backward:
 the fused query pass (D and dQ, recomputing S, P, dP) then the key pass
 storing no dS (no workspace), timed separately, with its own host-to-host
-``e2e`` (attn_step_host without a workspace).
+``e2e`` when the headline e2e took the stored order.
 
 ``--impl reference`` times the oracle (the CPU reference of this method) on
 the same workload, one bounded sample per step, and prints the same line
@@ -477,7 +479,8 @@ def run_ours(args, w, world, rank, local):
             raise RuntimeError("device error during the end-to-end steps")
         return dict(value=world * fl["step"] * Ke / (e_ms / 1e3) / 1e12, unit="TFLOP/s",
                     h2d_bytes_per_step=host.input_bytes(), d2h_bytes_per_step=host.output_bytes(),
-                    steps=Ke, ms_per_step=e_ms / Ke)
+                    steps=Ke, ms_per_step=e_ms / Ke,
+                    order=api.attn_step_host_order(s, api.device_buffers(dev_in, step_bufs)))
 
     e2e = None
     if not args.no_e2e:
@@ -501,10 +504,19 @@ def run_ours(args, w, world, rank, local):
             for _, fn in fcalls:
                 fn()
         Kf = max(1, min(K, 100))
+        # step-boundary events for the step time, then a per-call leg
+        fst = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(Kf)]
         fev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fcalls) + 1)]
                for _ in range(Kf)]
         dist_barrier(world)
         torch.cuda.synchronize(dev)
+        for i in range(Kf):
+            flush.zero_()
+            fst[i][0].record(stream)
+            for _, fn in fcalls:
+                fn()
+            fst[i][1].record(stream)
         for i in range(Kf):
             flush.zero_()
             fev[i][0].record(stream)
@@ -515,7 +527,7 @@ def run_ours(args, w, world, rank, local):
         dist_barrier(world)
         if api.last_device_error(stream) != 0:
             raise RuntimeError("device error during the fused-dQ steps")
-        f_ms = dist_max(sum(fev[i][0].elapsed_time(fev[i][-1]) for i in range(Kf)), world)
+        f_ms = dist_max(sum(a.elapsed_time(b) for a, b in fst), world)
         variant = dict(
             what="attn_fwd, attn_bwd_queries_fused (D and dQ, S, P, dP recomputed), then "
                  "attn_bwd_keys storing no dS: no workspace, no row-terms launch",
@@ -523,8 +535,9 @@ def run_ours(args, w, world, rank, local):
             ms_per_step=f_ms / Kf,
             kernels_ms={n: sum(fev[i][c].elapsed_time(fev[i][c + 1]) for i in range(Kf)) / Kf
                         for c, (n, _) in enumerate(fcalls)})
-        if host is not None:
-            # the same host-to-host step on this path (attn_step_host without a workspace)
+        if host is not None and e2e is not None and e2e["order"] == "stored":
+            # the host-to-host step in the fused order (attn_step_host without a
+            # workspace), when the headline e2e took the stored order
             variant["e2e"] = time_e2e(fbufs)
         del fbufs
 

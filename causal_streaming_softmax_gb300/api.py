@@ -27,6 +27,8 @@ ATTN_ERR_CUDA = -5
 ATTN_ERR_DEVICE_TIMEOUT = -6
 ATTN_ERR_DEVICE = -7
 ATTN_ERR_SCRATCH_LIMIT = -8
+ATTN_STEP_STORED = 0
+ATTN_STEP_FUSED = 1
 
 # lowest bounded-wait limit the library accepts (attn_set_wait_limit_ns)
 MIN_WAIT_LIMIT_NS = 10_000_000
@@ -107,6 +109,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attn_step_host.argtypes = [ctypes.POINTER(AttnShape), ctypes.POINTER(AttnDeviceBuffers)] + \
         [vp] * 10
     lib.attn_step_host.restype = ctypes.c_int
+    lib.attn_step_host_order.argtypes = [ctypes.POINTER(AttnShape),
+                                         ctypes.POINTER(AttnDeviceBuffers)]
+    lib.attn_step_host_order.restype = ctypes.c_int
     lib.attn_selftest_arith.restype = ctypes.c_int
     for name in ("attn_fwd", "attn_row_terms", "attn_bwd_keys", "attn_bwd_queries",
                  "attn_last_device_error", "attn_selftest_wait_timeout"):
@@ -426,20 +431,33 @@ class DeviceInputs:
         self.dout = torch.empty((B, H, T, 64), dtype=torch.float16, device=dev)
 
 
+def device_buffers(dev_in: DeviceInputs, bufs: Buffers) -> AttnDeviceBuffers:
+    return AttnDeviceBuffers(dev_in.q.data_ptr(), dev_in.k.data_ptr(), dev_in.vt.data_ptr(),
+                             dev_in.dout.data_ptr(), bufs.o.data_ptr(), bufs.lse.data_ptr(),
+                             bufs.delta.data_ptr(),
+                             None if bufs.ws is None else bufs.ws.data_ptr(),
+                             0 if bufs.ws is None else bufs.ws.numel() * bufs.ws.element_size(),
+                             bufs.dq.data_ptr(), bufs.dk.data_ptr(), bufs.dvt.data_ptr())
+
+
+def attn_step_host_order(s: Shape, dev: AttnDeviceBuffers) -> str:
+    """'stored' or 'fused': the order attn_step_host takes for ``s`` and ``dev``."""
+    shape = s.c_struct()
+    r = load_library().attn_step_host_order(ctypes.byref(shape), ctypes.byref(dev))
+    if r < 0:
+        raise AttnError("attn_step_host_order", r)
+    return "fused" if r == ATTN_STEP_FUSED else "stored"
+
+
 def attn_step_host(s: Shape, host: HostProblem, dev_in: DeviceInputs, bufs: Buffers,
                    stream=None) -> None:
     """Host-to-host pass through the C ABI: copies the inputs in, runs the
-    four calls and copies O, L, dQ, dK and dV^T back, the copies overlapped
-    with the kernels (asynchronous; synchronise the stream before reading
-    ``host``'s outputs).  ``bufs`` without a workspace selects the fused
-    query pass."""
-    dev = AttnDeviceBuffers(dev_in.q.data_ptr(), dev_in.k.data_ptr(), dev_in.vt.data_ptr(),
-                            dev_in.dout.data_ptr(), bufs.o.data_ptr(), bufs.lse.data_ptr(),
-                            bufs.delta.data_ptr(),
-                            None if bufs.ws is None else bufs.ws.data_ptr(),
-                            0 if bufs.ws is None else bufs.ws.numel() * bufs.ws.element_size(),
-                            bufs.dq.data_ptr(),
-                            bufs.dk.data_ptr(), bufs.dvt.data_ptr())
+    forward and backward calls and copies O, L, dQ, dK and dV^T back, the
+    copies overlapped with the kernels (asynchronous; synchronise the stream
+    before reading ``host``'s outputs).  ``bufs`` without a workspace, or a
+    dQ of 8 MiB or more, selects the fused query pass (attn_step_host_order
+    says which)."""
+    dev = device_buffers(dev_in, bufs)
     shape = s.c_struct()
     _check("attn_step_host", load_library().attn_step_host(
         ctypes.byref(shape), ctypes.byref(dev), host.q.data_ptr(), host.k.data_ptr(),

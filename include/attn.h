@@ -226,14 +226,29 @@ typedef struct attn_device_buffers {
  * before then.  Host buffers should be page-locked (pageable memory works,
  * but its copies do not overlap).  The shape must cover every K/V head
  * (head_begin = 0, head_count = 0 or Hkv); seq_lens, if any, is a device
- * array.  With dev->ws = NULL and dev->ws_bytes = 0 the step takes dQ from
- * attn_bwd_queries_fused and the key pass stores no dS (no workspace).  Errors as the calls above; a CUDA failure while enqueueing
+ * array.  The step takes dQ from attn_bwd_queries_fused, run before a key
+ * pass that stores no dS (no workspace needed), when dev->ws = NULL and
+ * dev->ws_bytes = 0, and also when dQ (B*H*T*64*4 bytes) is 8 MiB or more:
+ * dQ is then ready before the key pass and its copy back overlaps it, which
+ * measured faster end to end on every such workload (the host link bounds
+ * the step); smaller problems use the workspace and the stored order.
+ * Errors as the calls above; a CUDA failure while enqueueing
  * returns ATTN_ERR_CUDA with the work enqueued so far left on the streams.
  */
 ATTN_API int attn_step_host(const attn_shape* shape, const attn_device_buffers* dev,
                             const uint16_t* h_q, const uint16_t* h_k, const uint16_t* h_vt,
                             const uint16_t* h_dout, uint16_t* h_o, float* h_lse, float* h_dq,
                             float* h_dk, float* h_dvt, void* stream);
+
+/*
+ * attn_step_host_order - which order attn_step_host takes for this shape and
+ * these buffers: ATTN_STEP_STORED (row terms, the key pass storing dS, the dQ
+ * pass) or ATTN_STEP_FUSED (the fused query pass, then the key pass storing
+ * no dS).  Host only (nothing is launched or dereferenced but the two
+ * structs); ATTN_ERR_SHAPE or ATTN_ERR_NULL as attn_step_host would return.
+ */
+enum { ATTN_STEP_STORED = 0, ATTN_STEP_FUSED = 1 };
+ATTN_API int attn_step_host_order(const attn_shape* shape, const attn_device_buffers* dev);
 
 /*
  * dQ pass with the inverse half-split rotation in its epilogue (the rotated

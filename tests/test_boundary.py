@@ -140,6 +140,27 @@ def test_step_host_rejections(lib):
         api.ATTN_ERR_WORKSPACE
 
 
+def test_step_host_order(lib):
+    """attn_step_host takes the fused order without a workspace and for 8 MiB
+    of dQ or more, the stored order otherwise (host-side rule, no launch)."""
+    p = 0x1000
+    with_ws = api.AttnDeviceBuffers(p, p, p, p, p, p, p, p, 1 << 40, p, p, p)
+    no_ws = api.AttnDeviceBuffers(p, p, p, p, p, p, p, None, 0, p, p, p)
+    small = api.Shape(1, 256, 4, 2, causal=True)            # dQ 256 KiB
+    at_switch = api.Shape(1, 2048, 16, 4, causal=True)      # 8 MiB exactly: fused
+    below = api.Shape(1, 2048, 15, 5, causal=False)         # 7.5 MiB
+    assert api.attn_step_host_order(small, with_ws) == "stored"
+    assert api.attn_step_host_order(small, no_ws) == "fused"
+    assert api.attn_step_host_order(at_switch, with_ws) == "fused"
+    assert api.attn_step_host_order(below, with_ws) == "stored"
+    assert api.attn_step_host_order(api.Shape(4, 4096, 16, 16, causal=False), with_ws) == "fused"
+    s = shape()
+    assert lib.attn_step_host_order(ctypes.byref(s), None) == api.ATTN_ERR_NULL
+    bad = shape(heads=3)
+    assert lib.attn_step_host_order(ctypes.byref(bad), ctypes.byref(with_ws)) == \
+        api.ATTN_ERR_SHAPE
+
+
 def test_wait_limit_has_a_floor(lib):
     """The bounded-wait limit reads back as set, is raised to the floor when
     set lower, and 0 restores the default; no GPU is touched."""
@@ -158,7 +179,7 @@ def test_wait_limit_has_a_floor(lib):
 
 def test_header_constants_match_binding():
     text = open(os.path.join(ROOT, "include", "attn.h")).read()
-    codes = dict(re.findall(r"(ATTN_(?:OK|ERR_\w+))\s*=\s*(-?\d+)", text))
+    codes = dict(re.findall(r"(ATTN_(?:OK|ERR_\w+|STEP_\w+))\s*=\s*(-?\d+)", text))
     for name, value in codes.items():
         assert getattr(api, name) == int(value), name
     floor = re.search(r"ATTN_MIN_WAIT_LIMIT_NS\s+\(\(uint64_t\)(\d+)\)", text)

@@ -221,13 +221,23 @@ def test_workload_sampled(cuda_device, cfg):
     (2, 256, 2, 1, True, None),               # one K/V head: dQ in one piece
 ])
 def test_step_host_matches_device_path(cuda_device, B, T, H, Hkv, causal, lens, fused):
+    _step_host_against(B, T, H, Hkv, causal, lens, fused, fused)
+
+
+def test_step_host_large_dq_takes_fused_order(cuda_device):
+    """With a workspace but 8 MiB of dQ, attn_step_host runs the fused order:
+    the same bits as the forward, the fused query pass and the key pass."""
+    _step_host_against(1, 2048, 16, 4, True, None, False, True)
+
+
+def _step_host_against(B, T, H, Hkv, causal, lens, fused, expect_fused):
     """attn_step_host (host buffers in and out, copies overlapped with the
     kernels) gives the same bits as the four device calls, with the stored
     or the fused dQ pass."""
     import torch
     from causal_streaming_softmax_gb300 import api
     inp = workloads.make_custom_inputs(B, T, H, Hkv, causal=causal, lens=lens, seed=T + B)
-    ref = run_gpu(inp, causal=causal, fused_dq=fused)
+    ref = run_gpu(inp, causal=causal, fused_dq=expect_fused)
     ln = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
     s = api.Shape(B, T, H, Hkv, causal=causal, seq_lens=ln)
     host = api.HostProblem(s, *(torch.from_numpy(inp[n]) for n in ("q", "k", "vt", "dout")))
