@@ -81,6 +81,43 @@ def test_deterministic(cuda_device):
         assert np.array_equal(a[key], b[key], equal_nan=True), key
 
 
+@pytest.mark.parametrize("fused", [False, True])
+def test_back_to_back_steps_with_producer_kernels(cuda_device, fused):
+    """Every kernel may start while the one before it in the stream finishes
+    (programmatic dependent launch) and waits before touching memory.  Steps
+    run back to back with no host synchronisation, each fed by torch kernels
+    that write the inputs (and the sequence lengths) right before it, give
+    the same bits as steps run one at a time."""
+    import torch
+    from causal_streaming_softmax_gb300 import api
+    B, T, H, Hkv = 2, 640, 8, 2
+    sets = [workloads.make_custom_inputs(B, T, H, Hkv, causal=True, lens=ln, seed=40 + i)
+            for i, ln in enumerate(([640, 300], [129, 640], [640, 640]))]
+    ref = [run_gpu(x, causal=True, fused_dq=fused) for x in sets]
+    dev = "cuda"
+    src = [{n: torch.from_numpy(x[n]).to(dev) for n in ("q", "k", "vt", "dout")} for x in sets]
+    src_lens = [torch.tensor(x["lens"], dtype=torch.int32, device=dev) for x in sets]
+    q, k, vt, dout = (torch.empty_like(src[0][n]) for n in ("q", "k", "vt", "dout"))
+    lens = torch.empty_like(src_lens[0])
+    s = api.Shape(B, T, H, Hkv, causal=True, seq_lens=lens)
+    bufs = api.Buffers(s, workspace=not fused)
+    got = []
+    torch.cuda.synchronize()
+    for rep in range(2):
+        for i in range(len(sets)):
+            # torch kernels (not copies) write every input just before the step
+            for n, dst in (("q", q), ("k", k), ("vt", vt), ("dout", dout)):
+                torch.mul(src[i][n], 1.0, out=dst)
+            torch.add(src_lens[i], 0, out=lens)
+            api.forward_backward(s, q, k, vt, dout, bufs, fused_dq=fused)
+            got.append({n: getattr(bufs, n).clone() for n in ("o", "lse", "dq", "dk", "dvt")})
+    torch.cuda.synchronize()
+    assert api.last_device_error() == 0
+    for j, g in enumerate(got):
+        for n, v in g.items():
+            assert np.array_equal(v.cpu().numpy(), ref[j % len(sets)][n], equal_nan=True), (j, n)
+
+
 def test_head_chunks_match_whole(cuda_device):
     """The backward walked in K/V-head chunks (workspace per chunk) gives the
     same bits as one call over every head."""
@@ -277,6 +314,29 @@ def test_fused_dq_against_oracle(cuda_device, B, T, H, Hkv, causal, lens):
     inp = workloads.make_custom_inputs(B, T, H, Hkv, causal=causal, lens=lens, seed=T + 7 * H)
     gpu = run_gpu(inp, causal=causal, fused_dq=True)
     compare_full(gpu, _full(inp, causal), inp)
+
+
+@pytest.mark.parametrize("causal,Hkv", [(True, 4), (False, 16)])
+def test_fused_dq_persistent_against_oracle(cuda_device, causal, Hkv):
+    """Enough query tiles (at least two per SM) for the persistent fused query
+    pass, with a batch of two and a ragged last tile, element by element."""
+    B, T, H = 2, 1216, 16
+    inp = workloads.make_custom_inputs(B, T, H, Hkv, causal=causal, seed=77 + Hkv)
+    gpu = run_gpu(inp, causal=causal, fused_dq=True)
+    compare_full(gpu, _full(inp, causal), inp)
+
+
+def test_fused_dq_persistent_same_bits_as_per_tile_launch(cuda_device):
+    """Lengths equal to T take the one-CTA-per-tile kernel; without lengths the
+    same shape takes the persistent one: the products and sums are the same,
+    so are the bits."""
+    B, T, H, Hkv = 2, 1216, 16, 4
+    inp = workloads.make_custom_inputs(B, T, H, Hkv, causal=True, seed=81)
+    pers = run_gpu(inp, causal=True, fused_dq=True)
+    inp_l = dict(inp, lens=np.full(B, T, dtype=np.int32))
+    tile = run_gpu(inp_l, causal=True, fused_dq=True)
+    for name in ("o", "lse", "delta", "dq", "dk", "dvt"):
+        assert np.array_equal(pers[name], tile[name], equal_nan=True), name
 
 
 def test_fused_dq_sharp_softmax(cuda_device):
