@@ -411,6 +411,30 @@ def test_fused_dq_head_chunks_match_whole(cuda_device):
     assert np.array_equal(bufs.delta.cpu().numpy(), whole["delta"])
 
 
+def test_fused_dq_persistent_head_chunks_match_whole(cuda_device):
+    """The persistent fused query pass (at least two units per SM in every
+    chunk) walked in K/V-head chunks gives the same bits as one call."""
+    import torch
+    from causal_streaming_softmax_gb300 import api
+    B, T, H, Hkv = 2, 1216, 32, 8
+    inp = workloads.make_custom_inputs(B, T, H, Hkv, causal=True, seed=23)
+    whole = run_gpu(inp, causal=True, fused_dq=True)
+    dev = "cuda"
+    q, k, vt, dout = (torch.from_numpy(inp[n]).to(dev) for n in ("q", "k", "vt", "dout"))
+    s = api.Shape(B, T, H, Hkv, causal=True)
+    bufs = api.Buffers(s, workspace=False)
+    api.attn_fwd(s, q, k, vt, bufs.o, bufs.lse)
+    bufs.dq.fill_(float("nan"))
+    bufs.delta.fill_(float("nan"))
+    for begin, count in ((0, 4), (4, 4)):
+        api.attn_bwd_queries_fused(s.chunk(begin, count), q, k, vt, dout, bufs.o, bufs.lse,
+                                   bufs.delta, bufs.dq)
+    torch.cuda.synchronize()
+    assert api.last_device_error() == 0
+    assert np.array_equal(bufs.dq.cpu().numpy(), whole["dq"])
+    assert np.array_equal(bufs.delta.cpu().numpy(), whole["delta"])
+
+
 # ---------------------------------------------------------------------------
 # the dQ pass with the inverse half-split rotation (bfloat16, token-major)
 # ---------------------------------------------------------------------------
