@@ -556,6 +556,7 @@ def test_projection_epilogues(cuda_device, B, T, H, Hkv, causal, lens, store_ds)
 @pytest.mark.parametrize("B,T,H,Hkv,causal,lens", [
     (1, 512, 8, 2, True, None),
     (2, 320, 4, 4, False, [100, 320]),
+    (2, 1216, 16, 4, True, None),    # enough query tiles for the persistent passes
 ])
 def test_v_rows_layout(cuda_device, B, T, H, Hkv, causal, lens, fused):
     """The whole path with V as rows gives the same bits as with V^T (the
